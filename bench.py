@@ -1,0 +1,546 @@
+#!/usr/bin/env python
+"""Benchmark of the N:M SpMV decode path on one B300 (or N replicas).
+
+A "step" is one decode token's pass over the linear layers of one decoder
+block of the chosen workload (default: the Llama-3.1-8B-shaped block, 2:4,
+batch 1: q, k, v, o, gate, up, down) -- seven nm_spmv calls replayed from one
+CUDA graph.  Weights are synthetic (seeded N(0, 0.02), top-N |w| per group of
+M along K) and resident in HBM; three packed copies of the block rotate from
+step to step so that no step finds its weights in the 126 MB L2 (the
+rotation set is about 740 MB).
+
+Printed (rank 0, one JSON line): achieved GB/s of algorithmic bytes
+(kept values + mask bits + x + y) over the timed steps, microseconds per call
+per layer, the roofline of the SpMV kernel against the measured HBM peak,
+the dense fp16 cuBLAS GEMV of the same shapes, an end-to-end figure through
+the public API with host buffers, the CPU oracle as a reported baseline and
+the SM clocks seen during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import nm_synth  # noqa: E402
+
+METRIC = "N:M SpMV µs/call and achieved HBM GB/s (% of peak), batch-1 decode shapes"
+FALLBACK_HBM_GBS = 6400.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="llama31_8b_block", choices=sorted(nm_synth.WORKLOADS))
+    p.add_argument("--pattern", default=None, help="N:M, default: the workload's first")
+    p.add_argument("--batch", type=int, default=1)
+    p.add_argument("--copies", type=int, default=3, help="rotating packed copies (L2 defeat)")
+    p.add_argument("--profile-steps", type=int, default=50, help="steps of the per-call pass")
+    p.add_argument("--no-dense", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, reasons) while the GPU runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index, self.period_ms = index, period_ms
+        self.samples, self.proc, self.thread = [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sel = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not sel:
+            sel = [p for _, p in self.samples]
+            window = "whole run (timed region shorter than the sampling period)"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "nvidia-smi unavailable"}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in sel if num(p[1]) is not None]
+        mx = [num(p[2]) for p in sel if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in sel for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sel), "window": window}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def layer_list(wl):
+    return list(wl.all_layers()) if wl.blocks == 1 else list(wl.all_layers())[:7]
+
+
+# ------------------------------------------------------------------ workload
+
+def build_workload(wl, N, M, batch, copies, device="cuda", keep_dense=False):
+    """Generate, pack and replicate the layers of one step.  Returns a list of
+    dicts: name, rows, K, mats (packed copies), x, y, dense (optional)."""
+    from sparse_spmv_memory_02_b300 import nm
+    layers = []
+    for li, layer in layer_list(wl):
+        W, mask, x = nm_synth.layer_inputs(wl, li, layer, N, M, batch, device)
+        A = nm.nm_pack(W, mask, N, M)
+        mats = [A] + [nm.PackedMatrix(A.values.clone(), A.masks.clone(), A.rows, A.K, N, M)
+                      for _ in range(copies - 1)]
+        dense = None
+        if keep_dense:
+            Wm = torch.where(mask.bool(), W, torch.zeros((), dtype=W.dtype, device=device))
+            dense = [Wm] + [Wm.clone() for _ in range(copies - 1)]
+        del W, mask
+        y = torch.empty(batch, layer.rows, dtype=torch.float16, device=device)
+        layers.append(dict(name=layer.name, rows=layer.rows, K=layer.K, mats=mats,
+                           x=x if batch > 1 else x[0], y=y if batch > 1 else y[0], dense=dense,
+                           index=li))
+    torch.cuda.synchronize()
+    return layers
+
+
+def step_bytes(layers, batch):
+    from sparse_spmv_memory_02_b300.stream import algorithmic_bytes
+    return [algorithmic_bytes(L["mats"][0], batch, 2) for L in layers]
+
+
+def capture_step_graphs(layers, copies):
+    from sparse_spmv_memory_02_b300.stream import LayerStream
+    streams = []
+    for c in range(copies):
+        s = LayerStream([L["mats"][c] for L in layers], [L["x"] for L in layers],
+                        [L["y"] for L in layers])
+        s.capture()
+        streams.append(s)
+    return streams
+
+
+def per_call_pass(layers, copies, steps):
+    """One graph of `steps` steps with an external event between all calls;
+    returns the mean per-call device time (seconds) of every layer."""
+    from sparse_spmv_memory_02_b300 import nm
+    n = len(layers)
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(steps * n + 1)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            evs[0].record()
+            for s in range(steps):
+                for i, L in enumerate(layers):
+                    A = L["mats"][s % copies]
+                    if L["x"].dim() == 1:
+                        nm.nm_spmv(A, L["x"], L["y"])
+                    else:
+                        nm.nm_spmv_batched(A, L["x"], L["y"])
+                    evs[s * n + i + 1].record()
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    times = [[] for _ in range(n)]
+    for s in range(steps):
+        for i in range(n):
+            k = s * n + i
+            times[i].append(evs[k].elapsed_time(evs[k + 1]) * 1e-3)
+    del g
+    return [statistics.mean(t) for t in times], [statistics.median(t) for t in times]
+
+
+def dense_pass(layers, copies, steps, warmup):
+    """cuBLAS fp16 GEMV of W (dropped weights zeroed), same protocol."""
+    n = len(layers)
+    ys = [torch.empty_like(L["y"]) for L in layers]
+    graphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i, L in enumerate(layers):  # warm cuBLAS handles outside capture
+                torch.matmul(L["dense"][c], L["x"].t() if L["x"].dim() > 1 else L["x"])
+            with torch.cuda.graph(g, stream=side):
+                for i, L in enumerate(layers):
+                    if L["x"].dim() == 1:
+                        torch.mv(L["dense"][c], L["x"], out=ys[i])
+                    else:
+                        ys[i].copy_(torch.matmul(L["x"], L["dense"][c].t()))
+        torch.cuda.current_stream().wait_stream(side)
+        graphs.append(g)
+    for s in range(warmup):
+        graphs[s % copies].replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        graphs[s % copies].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    dt = e0.elapsed_time(e1) * 1e-3 / steps
+    dense_bytes = sum(L["rows"] * L["K"] * 2 for L in layers)
+    del graphs
+    return dt, dense_bytes, n
+
+
+def e2e_pass(layers, streams, copies, steps, warmup, batch):
+    """Through the public API with host buffers: per step, pinned-host x ->
+    device, the step's SpMV calls, device y -> pinned host, then the host
+    waits for y (a decode loop needs the result before the next token)."""
+    xs_h = [L["x"].detach().cpu().pin_memory() for L in layers]
+    ys_h = [torch.empty(L["y"].shape, dtype=L["y"].dtype).pin_memory() for L in layers]
+    h2d = sum(t.numel() * t.element_size() for t in xs_h)
+    d2h = sum(t.numel() * t.element_size() for t in ys_h)
+
+    def one(s):
+        for L, xh in zip(layers, xs_h):
+            L["x"].copy_(xh, non_blocking=True)
+        streams[s % copies].replay()
+        for L, yh in zip(layers, ys_h):
+            yh.copy_(L["y"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for s in range(warmup):
+        one(s)
+    t0 = time.perf_counter()
+    for s in range(steps):
+        one(s)
+    dt = (time.perf_counter() - t0) / steps
+    return dt, h2d, d2h
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_sample(wl, N, M, batch, row_fraction, device):
+    """Host copies for the oracle: the first ceil(rows * fraction) rows of
+    every layer of one step, packed by the oracle itself."""
+    import oracle
+    sample = []
+    for li, layer in layer_list(wl):
+        W, mask, x = nm_synth.layer_inputs(wl, li, layer, N, M, batch, device)
+        r = max(1, int(round(layer.rows * row_fraction)))
+        Wn = W[:r].cpu().numpy()
+        mn = mask[:r].cpu().numpy()
+        xn = x.cpu().numpy()
+        del W, mask
+        vals, masks, bad = oracle.pack(Wn, mn, N, M)
+        assert bad == 0
+        sample.append((vals, masks, layer.K, xn.view("uint16")))
+    return sample
+
+
+def run_oracle(sample, N, M, threads):
+    """Row ranges of every layer spread over host threads (the oracle's
+    arithmetic is untouched; ctypes releases the GIL).  Returns (seconds,
+    algorithmic bytes)."""
+    import numpy as np
+
+    import oracle
+    jobs, outs = [], []
+    for vals, masks, K, x in sample:
+        rows = vals.shape[0]
+        B = x.shape[0]
+        y = np.empty((B, rows))
+        s = np.empty((B, rows))
+        outs.append((y, s))
+        step = max(1, (rows + threads - 1) // threads)
+        for r0 in range(0, rows, step):
+            jobs.append((vals, masks, K, x, y, s, r0, min(rows, r0 + step)))
+    idx = [0]
+    lock = threading.Lock()
+
+    def worker():
+        while True:
+            with lock:
+                if idx[0] >= len(jobs):
+                    return
+                j = jobs[idx[0]]
+                idx[0] += 1
+            vals, masks, K, x, y, s, r0, r1 = j
+            oracle.spmv_packed_rows_into(vals, masks, K, N, M, x, y, s, r0, r1)
+
+    t0 = time.perf_counter()
+    ths = [threading.Thread(target=worker) for _ in range(threads)]
+    for t in ths:
+        t.start()
+    for t in ths:
+        t.join()
+    dt = time.perf_counter() - t0
+    nbytes = 0
+    for vals, masks, K, x in sample:
+        rows, B = vals.shape[0], x.shape[0]
+        nbytes += vals.size * 2 + rows * K // 8 + B * K * 2 + B * rows * 2
+    return dt, nbytes
+
+
+# ------------------------------------------------------------------ arms
+
+def config_block(args, wl, N, M, copies, layers_desc):
+    return {"workload": wl.key, "title": wl.title, "pattern": "%d:%d" % (N, M),
+            "batch": args.batch, "layers": layers_desc,
+            "l2": "rotating %d packed copies of the step's weights (> 3x the 126 MB L2)" % copies,
+            "launch": "one CUDA graph of %d nm_spmv calls per step" % len(layers_desc),
+            "weights": "synthetic N(0,0.02), top-N |w| per group of M along K",
+            "activations": "synthetic N(0,1), 1% outlier channels x20" if wl.outliers
+            else "synthetic N(0,1)"}
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores, on the same workload."""
+    if rank != 0:
+        return
+    wl = nm_synth.WORKLOADS[args.workload]
+    N, M = map(int, (args.pattern or "%d:%d" % wl.patterns[0]).split(":"))
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    threads = min(host_cores(), 64)
+    # each step: 1/32 of the rows of every layer of the step (a bounded sample)
+    frac = 1.0 / 32
+    sample = oracle_sample(wl, N, M, args.batch, frac, device)
+    for _ in range(args.warmup):
+        run_oracle(sample, N, M, threads)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = run_oracle(sample, N, M, threads)
+        tot_t += dt
+        tot_b += nb
+    gbs = tot_b / tot_t / 1e9
+    desc = [{"name": L.name, "rows": L.rows, "K": L.K} for _, L in layer_list(wl)]
+    out = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": tot_t / max(1, args.steps) * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": config_block(args, wl, N, M, 0, desc),
+           "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                            "sample": "first 1/32 of the rows of each layer per step"},
+           "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    from sparse_spmv_memory_02_b300 import build as nmbuild
+    nmbuild.build()
+    wl = nm_synth.WORKLOADS[args.workload]
+    N, M = map(int, (args.pattern or "%d:%d" % wl.patterns[0]).split(":"))
+    copies = max(1, args.copies)
+    layers = build_workload(wl, N, M, args.batch, copies, keep_dense=not args.no_dense)
+    bytes_per_call = step_bytes(layers, args.batch)
+    step_b = sum(bytes_per_call)
+    streams = capture_step_graphs(layers, copies)
+
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    for s in range(args.warmup):
+        streams[s % copies].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record()
+    for s in range(args.steps):
+        streams[s % copies].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    dt = e0.elapsed_time(e1) * 1e-3
+    dt = max_over_ranks(dt, world)
+    launches = len(layers) * args.steps
+
+    # per-call device times (events between the calls inside one graph)
+    mean_t, med_t = per_call_pass(layers, copies, min(args.profile_steps, max(3, args.steps)))
+    if sampler is not None:
+        sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+
+    dense = None
+    if not args.no_dense:
+        ddt, dbytes, _ = dense_pass(layers, copies, max(10, min(args.steps, 500)), args.warmup)
+        dense = {"us_per_step": ddt * 1e6, "dense_bytes_per_step": dbytes,
+                 "achieved_gbs": dbytes / ddt / 1e9,
+                 "speedup_sparse_vs_dense": ddt / (dt / args.steps),
+                 "kernel": "cuBLAS fp16 GEMV (torch.mv) on W with dropped weights zeroed"}
+        for L in layers:
+            L["dense"] = None
+        torch.cuda.empty_cache()
+
+    e2e = None
+    if not args.no_e2e:
+        et, h2d, d2h = e2e_pass(layers, streams, copies, max(10, min(args.steps, 500)),
+                                args.warmup, args.batch)
+        e2e = {"value": step_b / et / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "us_per_step": et * 1e6,
+               "path": "pinned host x -> device, graph of nm_spmv calls, y -> pinned host, "
+                       "host waits each step"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = min(host_cores(), 64)
+        sample = oracle_sample(wl, N, M, args.batch, 1.0, "cuda")
+        odt, ob = run_oracle(sample, N, M, threads)
+        cpu = {"value": ob / odt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": "one full step (all rows of the %d layers), row ranges over %d host "
+                         "threads, fp64" % (len(layers), threads),
+               "seconds": odt}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    total_kernel_t = sum(mean_t)
+    achieved = step_b / total_kernel_t / 1e9
+    value = world * step_b * args.steps / dt / 1e9
+    per_layer = {}
+    for L, b, mt, md in zip(layers, bytes_per_call, mean_t, med_t):
+        per_layer[L["name"]] = {"rows": L["rows"], "K": L["K"], "bytes": b, "us": mt * 1e6,
+                                "us_median": md * 1e6, "gbs": b / mt / 1e9,
+                                "frac_of_peak": b / mt / 1e9 / peak}
+    out = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "storage_dtype": "f16 values, 1-bit masks", "data": "synthetic",
+        "config": config_block(args, wl, N, M, copies,
+                               [{"name": L["name"], "rows": L["rows"], "K": L["K"]} for L in layers]),
+        "us_per_call": {k: v["us"] for k, v in per_layer.items()},
+        "per_layer": per_layer,
+        "step_algorithmic_bytes": step_b,
+        "frac_of_peak": value / world / peak,
+        "peak_gbs": peak, "peak_kind": peak_kind,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "nm_spmv_fast_kernel (all %d calls of a step)" % len(layers),
+                     "note": "achieved = algorithmic bytes of a step / sum of per-call device "
+                             "times (CUDA events between the calls, %s peak)" % peak_kind},
+        "dense_gemv": dense,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "gpu": torch.cuda.get_device_name(),
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_init()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

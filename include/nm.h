@@ -1,0 +1,162 @@
+/*
+ * nm.h -- C ABI of libnm: N:M structured-sparse matrix-vector products for
+ * token-by-token LLM decoding on NVIDIA B300 (sm_103a).
+ *
+ * What the library computes.  "SparseDecoding: Decoding-Aware Pruning for
+ * Accurate and Efficient LLM Inference" (Abstract) states that decoding is
+ * memory-bound and dominated by sparse matrix-vector (SpMV) products, and
+ * that its system contribution is an N:M sparse matrix-vector kernel with
+ * bitmask indexing and fixed-step traversal; "SparseDecoding Makes LLM
+ * Pruning Aware of Generation" (Key points) says the same.  The bedrocknews
+ * summary of arXiv 2610.12327v1 defines N:M structured sparsity as a fixed
+ * ratio of zeros inside small blocks and the product as a sparse matrix times
+ * a single vector.  The pages give no layout, interface or code; everything
+ * below that they do not state is this library's own reading of them.
+ *
+ * Packed layout (the "canonical layout"; pack output, SpMV input):
+ *   - W is rows x K (output features x input features), K a multiple of M.
+ *   - values: fp16, row-major [rows][K/M*N].  The N kept weights of group g
+ *     (positions g*M .. g*M+M-1 along K) sit at values[row][g*N + j],
+ *     j = 0..N-1, in increasing k.  Every group advances the value index by
+ *     exactly N, so no per-row offsets exist (fixed step).
+ *   - masks: uint32, row-major [rows][ceil(K/32)].  Bit b of word w is the
+ *     keep bit of position k = 32*w + b (least significant bit first); bits
+ *     past K are zero.  Because M divides 32, a group never spans two words.
+ *   - A valid matrix has exactly N set bits in every group.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named W, mask, values, masks, x, y are DEVICE pointers of the
+ *     calling thread's current CUDA device; the caller allocates, owns and
+ *     frees them.  The library keeps no pointer after a call returns.
+ *   - `stream` is a CUDA stream of that device (the same type as
+ *     cudaStream_t; NULL means the legacy default stream).  Work is ordered
+ *     on it.
+ *   - Supported patterns: M in {4, 8} and 1 <= N <= M.  Patterns with 8 % N
+ *     == 0 and K a multiple of 8*M/N take the vectorised kernel; the others
+ *     take a scalar kernel with the same results.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failing check returns NM_ERR_INVALID_ARG or NM_ERR_UNSUPPORTED and has
+ *     no effect.  A failing CUDA call returns NM_ERR_CUDA.  nm_last_error()
+ *     then describes the failure.  No C++ exception crosses this interface.
+ *   - rows == 0 is an empty problem: the call succeeds and does nothing.
+ */
+#ifndef NM_H_
+#define NM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NM_VERSION 100 /* 1.0.0 */
+#define NM_MAX_BATCH 8
+
+/* A CUDA stream handle; identical to cudaStream_t. */
+typedef struct CUstream_st *nm_stream_t;
+
+typedef enum nm_status {
+    NM_OK = 0,
+    NM_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or stride    */
+    NM_ERR_UNSUPPORTED = 2, /* N:M pattern outside M in {4,8}, 1 <= N <= M    */
+    NM_ERR_BAD_MASK = 3,    /* nm_pack: some group does not keep exactly N     */
+    NM_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed     */
+} nm_status;
+
+typedef enum nm_dtype {
+    NM_F16 = 0, /* IEEE binary16, rounded to nearest even */
+    NM_F32 = 1  /* IEEE binary32                          */
+} nm_dtype;
+
+/* A packed N:M matrix (see "Packed layout" above).  `values` and `masks`
+ * are device pointers owned by the caller; both must be 16-byte aligned. */
+typedef struct nm_matrix {
+    int64_t rows;            /* output features, >= 0                */
+    int64_t K;               /* input features, >= 0, multiple of M  */
+    int32_t N;               /* kept weights per group               */
+    int32_t M;               /* group length along K: 4 or 8         */
+    const void *values;      /* fp16 [rows][K/M*N]                   */
+    const uint32_t *masks;   /* uint32 [rows][ceil(K/32)]            */
+} nm_matrix;
+
+/*
+ * Byte sizes of the packed arrays for a rows x K matrix with pattern N:M
+ * (host only; no CUDA call).  values_bytes = rows*(K/M)*N*2,
+ * mask_bytes = rows*ceil(K/32)*4.  Either output pointer may be NULL.
+ * Errors: NM_ERR_INVALID_ARG for negative sizes, K not a multiple of M or
+ * a size that overflows size_t; NM_ERR_UNSUPPORTED for the pattern.
+ */
+nm_status nm_packed_sizes(int64_t rows, int64_t K, int N, int M,
+                          size_t *values_bytes, size_t *mask_bytes);
+
+/*
+ * Compress a dense fp16 matrix and its keep-mask into the packed layout
+ * (the representation step that "SparseDecoding: Why Pruning Should Account
+ * for How LLMs Generate", section 6, leaves open; bit-exact copy of the kept
+ * fp16 bit patterns, including -0.0, subnormals and NaN payloads).
+ *   W      fp16 [rows][K], row-major, device.
+ *   mask   uint8 [rows][K], row-major, device; nonzero = keep.  The mask, not
+ *          the value, decides what is kept: a kept zero is stored.
+ *   values fp16 [rows][K/M*N] and masks uint32 [rows][ceil(K/32)], device,
+ *          written completely (16-byte aligned).
+ * The call allocates a 4-byte device counter, validates every group and
+ * SYNCHRONISES `stream` to read it back, so it cannot be captured in a CUDA
+ * graph (capturing streams are refused with NM_ERR_INVALID_ARG).
+ * Returns NM_ERR_BAD_MASK if any group does not hold exactly N set bits; the
+ * outputs are then fully written but their contents are unspecified.
+ */
+nm_status nm_pack(const void *W, const uint8_t *mask, int64_t rows, int64_t K,
+                  int N, int M, void *values, uint32_t *masks, nm_stream_t stream);
+
+/*
+ * Expand a packed matrix back to dense fp16 [rows][K] (dropped positions
+ * become +0.0).  A test and debugging aid; asynchronous on `stream`.
+ * W_out: device, 2-byte aligned, rows*K*2 bytes, overwritten.
+ */
+nm_status nm_unpack(const nm_matrix *A, void *W_out, nm_stream_t stream);
+
+/*
+ * The decode-step product y = A x for one vector ("SparseDecoding:
+ * Decoding-Aware Pruning for Accurate and Efficient LLM Inference",
+ * Abstract: the N:M sparse matrix-vector kernel; bedrocknews summary of
+ * arXiv 2610.12327v1: a sparse matrix times a single vector).
+ *   A      packed matrix (host struct, device arrays).
+ *   x      fp16 [K], device, 16-byte aligned.
+ *   y      [rows] of y_type, device, naturally aligned; overwritten
+ *          (no alpha/beta).  If K == 0, y is set to zero.
+ * Products and sums are carried in fp32; y is rounded once at the end.
+ * Asynchronous: never synchronises, allocates nothing, and may be captured
+ * in a CUDA graph.  Results for a matrix with invalid groups are unspecified
+ * (never out of bounds).
+ */
+nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
+                  nm_stream_t stream);
+
+/*
+ * The same product for 1 <= batch <= NM_MAX_BATCH vectors sharing one pass
+ * over A (each weight byte is read once and used `batch` times).
+ *   x  fp16 [batch][ldx], device; ldx >= K; with batch > 1, ldx must be a
+ *      multiple of 8 so that every vector starts 16-byte aligned.
+ *   y  y_type [batch][ldy], device; ldy >= rows.  Row b of y receives A x_b.
+ * Same semantics and errors as nm_spmv.
+ */
+nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
+                          void *y, int64_t ldy, int batch, nm_dtype y_type,
+                          nm_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *nm_status_str(nm_status status);
+
+/* Description of the last failing call on the calling thread ("" if none).
+ * The pointer stays valid until the thread's next libnm call. */
+const char *nm_last_error(void);
+
+/* NM_VERSION of the loaded library. */
+int nm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NM_H_ */

@@ -1,0 +1,247 @@
+// C entry points of libnm (declared in include/nm.h): argument checks on the
+// host, then one kernel launch.  No exception crosses this file's functions.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+
+#include "nm.h"
+#include "nm_internal.h"
+
+namespace nm {
+cudaError_t launch_fast_1_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_fast_2_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_fast_4_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_fast_1_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_fast_2_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_fast_4_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_fast_8_8(const SpmvProblem &, cudaStream_t);
+
+bool fast_path_applies(int N, int M, int64_t K)
+{
+    if (M != 4 && M != 8) return false;
+    if (N < 1 || N > M || 8 % N != 0) return false;
+    const int64_t ck = 8 * M / N;  // positions covered by one 16-byte value chunk
+    return K > 0 && K % ck == 0 && K / ck <= INT_MAX / 2;
+}
+
+cudaError_t launch_fast(const SpmvProblem &p, cudaStream_t s)
+{
+    switch (p.M * 16 + p.N) {
+    case 4 * 16 + 1: return launch_fast_1_4(p, s);
+    case 4 * 16 + 2: return launch_fast_2_4(p, s);
+    case 4 * 16 + 4: return launch_fast_4_4(p, s);
+    case 8 * 16 + 1: return launch_fast_1_8(p, s);
+    case 8 * 16 + 2: return launch_fast_2_8(p, s);
+    case 8 * 16 + 4: return launch_fast_4_8(p, s);
+    case 8 * 16 + 8: return launch_fast_8_8(p, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace nm
+
+namespace {
+
+thread_local char g_last_error[512];
+
+nm_status fail(nm_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+nm_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(NM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// rows and K bounds keep every index of the kernels inside int64 and the
+// per-launch row count inside int.
+constexpr int64_t kMaxRows = INT_MAX;
+constexpr int64_t kMaxK = INT_MAX;
+
+nm_status check_shape(int64_t rows, int64_t K, int N, int M)
+{
+    if (M != 4 && M != 8) return fail(NM_ERR_UNSUPPORTED, "M=%d: only M in {4, 8} is supported", M);
+    if (N < 1 || N > M)
+        return fail(NM_ERR_UNSUPPORTED, "N=%d: need 1 <= N <= M (M=%d)", N, M);
+    if (rows < 0 || K < 0) return fail(NM_ERR_INVALID_ARG, "negative size rows=%lld K=%lld",
+                                       (long long)rows, (long long)K);
+    if (rows > kMaxRows || K > kMaxK)
+        return fail(NM_ERR_INVALID_ARG, "size too large rows=%lld K=%lld (max %lld each)",
+                    (long long)rows, (long long)K, (long long)INT_MAX);
+    if (K % M != 0)
+        return fail(NM_ERR_INVALID_ARG, "K=%lld is not a multiple of M=%d", (long long)K, M);
+    return NM_OK;
+}
+
+nm_status check_matrix(const nm_matrix *A)
+{
+    if (!A) return fail(NM_ERR_INVALID_ARG, "matrix descriptor is NULL");
+    nm_status st = check_shape(A->rows, A->K, A->N, A->M);
+    if (st != NM_OK) return st;
+    if (A->rows > 0 && A->K > 0) {
+        if (!A->values || !A->masks) return fail(NM_ERR_INVALID_ARG, "values or masks is NULL");
+        if (!aligned(A->values, 16) || !aligned(A->masks, 16))
+            return fail(NM_ERR_INVALID_ARG, "values and masks must be 16-byte aligned");
+    }
+    return NM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int nm_version(void) { return NM_VERSION; }
+
+const char *nm_last_error(void) { return g_last_error; }
+
+const char *nm_status_str(nm_status status)
+{
+    switch (status) {
+    case NM_OK: return "NM_OK";
+    case NM_ERR_INVALID_ARG: return "NM_ERR_INVALID_ARG";
+    case NM_ERR_UNSUPPORTED: return "NM_ERR_UNSUPPORTED";
+    case NM_ERR_BAD_MASK: return "NM_ERR_BAD_MASK";
+    case NM_ERR_CUDA: return "NM_ERR_CUDA";
+    default: return "NM_ERR_UNKNOWN";
+    }
+}
+
+nm_status nm_packed_sizes(int64_t rows, int64_t K, int N, int M, size_t *values_bytes,
+                          size_t *mask_bytes)
+{
+    g_last_error[0] = 0;
+    nm_status st = check_shape(rows, K, N, M);
+    if (st != NM_OK) return st;
+    // rows, K < 2^31, so every product below stays under 2^63.
+    const int64_t vb = rows * ((K / M) * N) * 2;
+    const int64_t mb = rows * ((K + 31) / 32) * 4;
+    if (values_bytes) *values_bytes = static_cast<size_t>(vb);
+    if (mask_bytes) *mask_bytes = static_cast<size_t>(mb);
+    return NM_OK;
+}
+
+nm_status nm_pack(const void *W, const uint8_t *mask, int64_t rows, int64_t K, int N, int M,
+                  void *values, uint32_t *masks, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    nm_status st = check_shape(rows, K, N, M);
+    if (st != NM_OK) return st;
+    if (rows == 0 || K == 0) return NM_OK;
+    if (!W || !mask || !values || !masks)
+        return fail(NM_ERR_INVALID_ARG, "W, mask, values and masks must be non-NULL");
+    if (!aligned(W, 2)) return fail(NM_ERR_INVALID_ARG, "W must be 2-byte aligned");
+    if (!aligned(values, 16) || !aligned(masks, 16))
+        return fail(NM_ERR_INVALID_ARG, "values and masks must be 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_pack: cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(NM_ERR_INVALID_ARG, "nm_pack synchronises its stream and cannot be captured");
+
+    unsigned int *d_bad = nullptr;
+    e = cudaMallocAsync(reinterpret_cast<void **>(&d_bad), sizeof(unsigned int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_pack: cudaMallocAsync");
+    unsigned int h_bad = 0;
+    e = cudaMemsetAsync(d_bad, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess)
+        e = nm::launch_pack(static_cast<const uint16_t *>(W), mask, rows, K, N, M,
+                            static_cast<uint16_t *>(values), masks, d_bad, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&h_bad, d_bad, sizeof(unsigned int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaError_t ef = cudaFreeAsync(d_bad, s);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_pack");
+    if (ef != cudaSuccess) return cuda_fail(ef, "nm_pack: cudaFreeAsync");
+    if (h_bad != 0)
+        return fail(NM_ERR_BAD_MASK, "%u group(s) do not keep exactly N=%d of M=%d", h_bad, N, M);
+    return NM_OK;
+}
+
+nm_status nm_unpack(const nm_matrix *A, void *W_out, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    nm_status st = check_matrix(A);
+    if (st != NM_OK) return st;
+    if (A->rows == 0 || A->K == 0) return NM_OK;
+    if (!W_out) return fail(NM_ERR_INVALID_ARG, "W_out is NULL");
+    if (!aligned(W_out, 2)) return fail(NM_ERR_INVALID_ARG, "W_out must be 2-byte aligned");
+    cudaError_t e = nm::launch_unpack(static_cast<const uint16_t *>(A->values), A->masks, A->rows,
+                                      A->K, A->N, A->M, static_cast<uint16_t *>(W_out),
+                                      reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "nm_unpack launch");
+    return NM_OK;
+}
+
+nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx, void *y, int64_t ldy,
+                          int batch, nm_dtype y_type, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    nm_status st = check_matrix(A);
+    if (st != NM_OK) return st;
+    if (batch < 1 || batch > NM_MAX_BATCH)
+        return fail(NM_ERR_INVALID_ARG, "batch=%d outside [1, %d]", batch, NM_MAX_BATCH);
+    if (y_type != NM_F16 && y_type != NM_F32)
+        return fail(NM_ERR_INVALID_ARG, "unknown y_type %d", (int)y_type);
+    const size_t esize = y_type == NM_F32 ? 4 : 2;
+    if (ldy < A->rows)
+        return fail(NM_ERR_INVALID_ARG, "ldy=%lld < rows=%lld", (long long)ldy, (long long)A->rows);
+    if (A->K > 0) {
+        if (ldx < A->K)
+            return fail(NM_ERR_INVALID_ARG, "ldx=%lld < K=%lld", (long long)ldx, (long long)A->K);
+        if (batch > 1 && ldx % 8 != 0)
+            return fail(NM_ERR_INVALID_ARG, "ldx=%lld must be a multiple of 8 when batch > 1",
+                        (long long)ldx);
+    }
+    if (A->rows == 0) return NM_OK;
+    if (!y) return fail(NM_ERR_INVALID_ARG, "y is NULL");
+    if (!aligned(y, esize)) return fail(NM_ERR_INVALID_ARG, "y is not %zu-byte aligned", esize);
+    if (ldy > (INT64_MAX / 16) / batch) return fail(NM_ERR_INVALID_ARG, "ldy too large");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (A->K == 0) {  // empty sums: y = 0
+        cudaError_t e = cudaMemset2DAsync(y, static_cast<size_t>(ldy) * esize, 0,
+                                          static_cast<size_t>(A->rows) * esize, batch, s);
+        if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: cudaMemset2DAsync");
+        return NM_OK;
+    }
+    if (!x) return fail(NM_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned(x, 16)) return fail(NM_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    if (ldx > (INT64_MAX / 16) / batch) return fail(NM_ERR_INVALID_ARG, "ldx too large");
+
+    nm::SpmvProblem p;
+    p.rows = A->rows;
+    p.K = A->K;
+    p.N = A->N;
+    p.M = A->M;
+    p.values = A->values;
+    p.masks = A->masks;
+    p.x = x;
+    p.ldx = ldx;
+    p.y = y;
+    p.ldy = ldy;
+    p.batch = batch;
+    p.y_f32 = y_type == NM_F32;
+    cudaError_t e = nm::fast_path_applies(p.N, p.M, p.K) ? nm::launch_fast(p, s)
+                                                         : nm::launch_generic(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv launch");
+    return NM_OK;
+}
+
+nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type, nm_stream_t stream)
+{
+    if (!A) {
+        g_last_error[0] = 0;
+        return fail(NM_ERR_INVALID_ARG, "matrix descriptor is NULL");
+    }
+    return nm_spmv_batched(A, x, A->K, y, A->rows, 1, y_type, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// Internal interface between the C entry points (nm_api.cu) and the kernel
+// launchers.  Not installed; the public interface is include/nm.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nm.h"
+
+namespace nm {
+
+// One product y[b] = A x[b] for b < batch, arguments already validated.
+struct SpmvProblem {
+    int64_t rows;
+    int64_t K;
+    int N;
+    int M;
+    const void *values;
+    const uint32_t *masks;
+    const void *x;
+    int64_t ldx;
+    void *y;
+    int64_t ldy;
+    int batch;
+    bool y_f32;
+};
+
+// Vectorised kernel: 8 % N == 0 and K a multiple of the k-span of one
+// 16-byte value chunk (8*M/N positions), and at most kMaxFastChunks chunks
+// per K tile sweep (any K is handled by tiling K inside a block).
+bool fast_path_applies(int N, int M, int64_t K);
+cudaError_t launch_fast(const SpmvProblem &p, cudaStream_t s);
+
+// Scalar kernel for every valid pattern and K (patterns like 3:4, or K not
+// a multiple of the chunk span).
+cudaError_t launch_generic(const SpmvProblem &p, cudaStream_t s);
+
+// Pack / unpack kernels.  `bad` counts groups whose mask is not exactly N.
+cudaError_t launch_pack(const uint16_t *W, const uint8_t *mask, int64_t rows, int64_t K,
+                        int N, int M, uint16_t *values, uint32_t *masks,
+                        unsigned int *bad, cudaStream_t s);
+cudaError_t launch_unpack(const uint16_t *values, const uint32_t *masks, int64_t rows,
+                          int64_t K, int N, int M, uint16_t *W, cudaStream_t s);
+
+// Cached device attributes of the current device.
+int sm_count();
+
+}  // namespace nm

@@ -1,0 +1,197 @@
+"""Thin ctypes binding of libnm (include/nm.h) for PyTorch tensors.
+
+Argument marshalling only: every step of the product runs in libnm's CUDA
+kernels.  Tensors supply device memory (``data_ptr()``) and the calls are
+ordered on ``torch.cuda.current_stream()`` unless a stream is given.  If the
+shared library is missing the import of this module's functions fails
+loudly; there is no CPU fallback.
+
+The names mirror the C interface: nm_packed_sizes, nm_pack, nm_unpack,
+nm_spmv, nm_spmv_batched, nm_status_str, nm_last_error, nm_version.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnm.so")
+
+NM_OK, NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_BAD_MASK, NM_ERR_CUDA = 0, 1, 2, 3, 4
+NM_F16, NM_F32 = 0, 1
+NM_MAX_BATCH = 8
+
+
+class NMError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_status_name(status), message))
+        self.status = status
+
+
+class nm_matrix(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("K", ctypes.c_int64), ("N", ctypes.c_int32),
+                ("M", ctypes.c_int32), ("values", ctypes.c_void_p), ("masks", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libnm.so with argument types declared (raises if absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    "libnm.so not found at %s; build it with "
+                    "`python -m sparse_spmv_memory_02_b300.build`" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            mp = ctypes.POINTER(nm_matrix)
+            L.nm_packed_sizes.argtypes = [i64, i64, i32, i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+            L.nm_pack.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp]
+            L.nm_unpack.argtypes = [mp, vp, vp]
+            L.nm_spmv.argtypes = [mp, vp, vp, i32, vp]
+            L.nm_spmv_batched.argtypes = [mp, vp, i64, vp, i64, i32, i32, vp]
+            for f in (L.nm_packed_sizes, L.nm_pack, L.nm_unpack, L.nm_spmv, L.nm_spmv_batched):
+                f.restype = ctypes.c_int
+            L.nm_status_str.argtypes = [ctypes.c_int]
+            L.nm_status_str.restype = ctypes.c_char_p
+            L.nm_last_error.argtypes = []
+            L.nm_last_error.restype = ctypes.c_char_p
+            L.nm_version.argtypes = []
+            L.nm_version.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return lib().nm_status_str(status).decode()
+    except Exception:
+        return "NM_STATUS_%d" % status
+
+
+def nm_status_str(status: int) -> str:
+    return lib().nm_status_str(status).decode()
+
+
+def nm_last_error() -> str:
+    return lib().nm_last_error().decode()
+
+
+def nm_version() -> int:
+    return lib().nm_version()
+
+
+def _check(status: int):
+    if status != NM_OK:
+        raise NMError(status, nm_last_error())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check_vec(t, name):
+    if t.dtype != torch.float16:
+        raise TypeError("%s must be float16, got %s" % (name, t.dtype))
+    if t.dim() > 0 and t.stride(-1) != 1:
+        raise ValueError("%s must have unit stride along K" % name)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+@dataclass
+class PackedMatrix:
+    """A packed N:M matrix on the GPU: values fp16 [rows][K/M*N] and masks
+    uint32 [rows][ceil(K/32)] (the layout of include/nm.h)."""
+    values: torch.Tensor
+    masks: torch.Tensor
+    rows: int
+    K: int
+    N: int
+    M: int
+
+    def __post_init__(self):
+        self._desc = nm_matrix(self.rows, self.K, self.N, self.M,
+                               _ptr(self.values), _ptr(self.masks))
+
+    @property
+    def desc(self) -> nm_matrix:
+        return self._desc
+
+    @property
+    def nbytes(self) -> int:
+        return self.values.numel() * 2 + self.masks.numel() * 4
+
+
+def nm_packed_sizes(rows: int, K: int, N: int, M: int):
+    vb, mb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().nm_packed_sizes(rows, K, N, M, ctypes.byref(vb), ctypes.byref(mb)))
+    return vb.value, mb.value
+
+
+def nm_pack(W: torch.Tensor, mask: torch.Tensor, N: int, M: int,
+            values: torch.Tensor | None = None, masks: torch.Tensor | None = None,
+            stream=None) -> PackedMatrix:
+    """Pack dense fp16 W [rows][K] with its uint8 keep-mask (synchronises)."""
+    rows, K = W.shape
+    vb, mb = nm_packed_sizes(rows, K, N, M)
+    if values is None:
+        values = torch.empty(vb // 2, dtype=torch.float16, device=W.device).view(rows, -1) \
+            if rows else torch.empty(0, (K // M) * N, dtype=torch.float16, device=W.device)
+    if masks is None:
+        masks = torch.empty(mb // 4, dtype=torch.int32, device=W.device).view(rows, -1) \
+            if rows else torch.empty(0, (K + 31) // 32, dtype=torch.int32, device=W.device)
+    _check(lib().nm_pack(_ptr(W), _ptr(mask), rows, K, N, M, _ptr(values), _ptr(masks),
+                         _stream(stream)))
+    return PackedMatrix(values, masks, rows, K, N, M)
+
+
+def nm_unpack(A: PackedMatrix, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(A.rows, A.K, dtype=torch.float16, device=A.values.device)
+    _check(lib().nm_unpack(ctypes.byref(A.desc), _ptr(out), _stream(stream)))
+    return out
+
+
+def nm_spmv(A: PackedMatrix, x: torch.Tensor, y: torch.Tensor | None = None,
+            y_dtype=torch.float16, stream=None) -> torch.Tensor:
+    """y = A x for one fp16 vector x [K]."""
+    _check_vec(x, "x")
+    if x.shape[-1] < A.K:
+        raise ValueError("x has %d entries, the matrix needs K=%d" % (x.shape[-1], A.K))
+    if y is None:
+        y = torch.empty(A.rows, dtype=y_dtype, device=x.device)
+    yt = NM_F32 if y.dtype == torch.float32 else NM_F16
+    _check(lib().nm_spmv(ctypes.byref(A.desc), _ptr(x), _ptr(y), yt, _stream(stream)))
+    return y
+
+
+def nm_spmv_batched(A: PackedMatrix, x: torch.Tensor, y: torch.Tensor | None = None,
+                    y_dtype=torch.float16, stream=None) -> torch.Tensor:
+    """y[b] = A x[b] for x [batch][ldx] (row stride = x.stride(0))."""
+    _check_vec(x, "x")
+    batch = x.shape[0]
+    ldx = x.stride(0) if batch > 1 else x.shape[1]
+    if y is None:
+        y = torch.empty(batch, A.rows, dtype=y_dtype, device=x.device)
+    ldy = y.stride(0) if batch > 1 else y.shape[-1]
+    yt = NM_F32 if y.dtype == torch.float32 else NM_F16
+    _check(lib().nm_spmv_batched(ctypes.byref(A.desc), _ptr(x), ldx, _ptr(y), ldy, batch, yt,
+                                 _stream(stream)))
+    return y

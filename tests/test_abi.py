@@ -1,0 +1,158 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/nm.h declares, and rejects bad arguments on the host before any CUDA
+call is made (so these checks need no device)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from sparse_spmv_memory_02_b300 import build as nmbuild
+from sparse_spmv_memory_02_b300 import nm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nm.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nmbuild.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nm_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_interface():
+    assert {"nm_packed_sizes", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_batched",
+            "nm_status_str", "nm_last_error", "nm_version"} <= set(declared_functions())
+
+
+def test_library_exports_every_declared_symbol():
+    out = subprocess.run(["nm", "-D", "--defined-only", nm.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(nm_\w+)$", out, flags=re.M))
+    missing = [f for f in declared_functions() if f not in exported]
+    assert not missing, missing
+    L = nm.lib()
+    for f in declared_functions():
+        assert hasattr(L, f)
+
+
+def test_version_and_status_strings():
+    assert nm.nm_version() == int(re.search(r"#define NM_VERSION (\d+)", open(HEADER).read()).group(1))
+    names = [nm.nm_status_str(s) for s in range(5)]
+    assert names == ["NM_OK", "NM_ERR_INVALID_ARG", "NM_ERR_UNSUPPORTED", "NM_ERR_BAD_MASK",
+                     "NM_ERR_CUDA"]
+    assert nm.nm_status_str(99) == "NM_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("rows,K,N,M", [(4096, 4096, 2, 4), (3, 12, 2, 4), (5, 40, 4, 8),
+                                        (1, 8, 1, 8), (0, 64, 2, 4), (7, 0, 2, 4)])
+def test_packed_sizes(rows, K, N, M):
+    vb, mb = nm.nm_packed_sizes(rows, K, N, M)
+    assert vb == rows * (K // M) * N * 2
+    assert mb == rows * ((K + 31) // 32) * 4
+
+
+@pytest.mark.parametrize("rows,K,N,M,status", [
+    (4, 16, 2, 16, nm.NM_ERR_UNSUPPORTED),
+    (4, 16, 0, 4, nm.NM_ERR_UNSUPPORTED),
+    (4, 16, 5, 4, nm.NM_ERR_UNSUPPORTED),
+    (4, 18, 2, 4, nm.NM_ERR_INVALID_ARG),
+    (-1, 16, 2, 4, nm.NM_ERR_INVALID_ARG),
+    (4, -8, 2, 4, nm.NM_ERR_INVALID_ARG),
+    (2 ** 31, 16, 2, 4, nm.NM_ERR_INVALID_ARG),
+])
+def test_packed_sizes_errors(rows, K, N, M, status):
+    with pytest.raises(nm.NMError) as e:
+        nm.nm_packed_sizes(rows, K, N, M)
+    assert e.value.status == status
+    assert nm.nm_last_error()
+
+
+# Fake device addresses: the checks below fail before anything touches them.
+A16, B16, C16, D16 = 0x10000, 0x20000, 0x30000, 0x40000
+
+
+def _mat(rows=64, K=256, N=2, M=4, values=A16, masks=B16):
+    return nm.nm_matrix(rows, K, N, M, values, masks)
+
+
+def _spmv_b(mat, x=C16, ldx=None, y=D16, ldy=None, batch=1, yt=nm.NM_F16):
+    ldx = mat.K if ldx is None else ldx
+    ldy = mat.rows if ldy is None else ldy
+    return nm.lib().nm_spmv_batched(ctypes.byref(mat), x, ldx, y, ldy, batch, yt, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(batch=0), nm.NM_ERR_INVALID_ARG),
+    (dict(batch=9), nm.NM_ERR_INVALID_ARG),
+    (dict(yt=7), nm.NM_ERR_INVALID_ARG),
+    (dict(ldx=255), nm.NM_ERR_INVALID_ARG),
+    (dict(ldy=63), nm.NM_ERR_INVALID_ARG),
+    (dict(batch=2, ldx=260), nm.NM_ERR_INVALID_ARG),      # ldx not a multiple of 8
+    (dict(x=0), nm.NM_ERR_INVALID_ARG),
+    (dict(y=0), nm.NM_ERR_INVALID_ARG),
+    (dict(x=C16 + 8), nm.NM_ERR_INVALID_ARG),             # x not 16-byte aligned
+    (dict(y=D16 + 1), nm.NM_ERR_INVALID_ARG),             # y not 2-byte aligned
+    (dict(y=D16 + 2, yt=nm.NM_F32), nm.NM_ERR_INVALID_ARG),
+])
+def test_spmv_batched_rejects_bad_arguments(kwargs, status):
+    assert _spmv_b(_mat(), **kwargs) == status
+    assert nm.nm_last_error() != ""
+
+
+@pytest.mark.parametrize("mat,status", [
+    (_mat(M=16), nm.NM_ERR_UNSUPPORTED),
+    (_mat(N=0), nm.NM_ERR_UNSUPPORTED),
+    (_mat(N=9, M=8), nm.NM_ERR_UNSUPPORTED),
+    (_mat(K=258), nm.NM_ERR_INVALID_ARG),
+    (_mat(rows=-1), nm.NM_ERR_INVALID_ARG),
+    (_mat(values=0), nm.NM_ERR_INVALID_ARG),
+    (_mat(masks=0), nm.NM_ERR_INVALID_ARG),
+    (_mat(values=A16 + 2), nm.NM_ERR_INVALID_ARG),
+    (_mat(masks=B16 + 4), nm.NM_ERR_INVALID_ARG),
+])
+def test_spmv_rejects_bad_matrix(mat, status):
+    assert nm.lib().nm_spmv(ctypes.byref(mat), C16, D16, nm.NM_F16, None) == status
+    assert nm.lib().nm_unpack(ctypes.byref(mat), D16, None) == status
+
+
+def test_null_descriptor():
+    L = nm.lib()
+    assert L.nm_spmv(None, C16, D16, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_batched(None, C16, 256, D16, 64, 1, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_unpack(None, D16, None) == nm.NM_ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_no_op_without_touching_memory():
+    # rows == 0: nothing is launched, so even NULL arrays are accepted
+    m = nm.nm_matrix(0, 256, 2, 4, 0, 0)
+    assert nm.lib().nm_spmv(ctypes.byref(m), 0, 0, nm.NM_F16, None) == nm.NM_OK
+    assert nm.lib().nm_pack(0, 0, 0, 256, 2, 4, 0, 0, None) == nm.NM_OK
+    assert nm.lib().nm_pack(0, 0, 5, 0, 2, 4, 0, 0, None) == nm.NM_OK
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A16, B16, 4, 16, 2, 3, C16, D16), nm.NM_ERR_UNSUPPORTED),
+    ((A16, B16, 4, 18, 2, 4, C16, D16), nm.NM_ERR_INVALID_ARG),
+    ((0, B16, 4, 16, 2, 4, C16, D16), nm.NM_ERR_INVALID_ARG),
+    ((A16, 0, 4, 16, 2, 4, C16, D16), nm.NM_ERR_INVALID_ARG),
+    ((A16, B16, 4, 16, 2, 4, 0, D16), nm.NM_ERR_INVALID_ARG),
+    ((A16 + 1, B16, 4, 16, 2, 4, C16, D16), nm.NM_ERR_INVALID_ARG),
+    ((A16, B16, 4, 16, 2, 4, C16 + 2, D16), nm.NM_ERR_INVALID_ARG),
+    ((A16, B16, 4, 16, 2, 4, C16, D16 + 4), nm.NM_ERR_INVALID_ARG),
+])
+def test_pack_rejects_bad_arguments(args, status):
+    assert nm.lib().nm_pack(*args, None) == status
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(nm, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(nm, "_lib", None)
+    with pytest.raises(ImportError):
+        nm.lib()
