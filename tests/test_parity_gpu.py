@@ -97,9 +97,9 @@ def test_pack_unpack_bit_exact(N, M, rows, K):
 
 def test_pack_special_bit_patterns():
     rows, K, N, M = 4, 64, 2, 4
-    bits = torch.tensor([0x8000, 0x0000, 0x7C00, 0xFC00, 0x0001, 0x7BFF, 0x7E01, 0x3C00],
-                        dtype=torch.int16).repeat(rows, K // 8)
-    W = bits.view(torch.float16).to(DEV)
+    bits = np.array([0x8000, 0x0000, 0x7C00, 0xFC00, 0x0001, 0x7BFF, 0x7E01, 0x3C00],
+                    dtype=np.uint16)
+    W = torch.from_numpy(np.tile(bits, (rows, K // 8)).view(np.float16)).to(DEV)
     mask = nm_synth.random_mask(rows, K, N, M, 3, DEV)
     _pack_and_check(W, mask, N, M)
 
