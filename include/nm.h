@@ -110,6 +110,33 @@ nm_status nm_pack(const void *W, const uint8_t *mask, int64_t rows, int64_t K,
                   int N, int M, void *values, uint32_t *masks, nm_stream_t stream);
 
 /*
+ * nm_pack for callers that cannot let a library allocate device memory.
+ * The pages have no counterpart to this call; it exists for deployment.
+ * Who needs it: an engine that reserves almost all device memory for its
+ * own pools before loading this library (an extra allocation would fail or
+ * fragment them), a runtime with a fixed device-memory budget, or code that
+ * must not risk the implicit device synchronisation an allocation or a free
+ * can cause.  nm_pack needs four bytes of device scratch (its bad-group
+ * counter) and allocates them on every call; this variant counts into a
+ * static array of NM_NOALLOC_SCRATCH_BYTES bytes compiled into the library
+ * (present on every GPU that loads the library, until the process exits)
+ * and calls no allocating routine.
+ *   Arguments, layout, results and errors are those of nm_pack, plus:
+ *   - rows*(K/M) above NM_PACK_NOALLOC_MAX_GROUPS (what the 32-bit counter
+ *     can count) is rejected with NM_ERR_INVALID_ARG;
+ *   - the first call on a device, made with that device current, looks up
+ *     the array's device address (cudaGetSymbolAddress) and caches it; make
+ *     that first call before any stream capture;
+ *   - every call on a device shares the array and clears the counter first;
+ *     two calls that overlap on the GPU (for example on different streams)
+ *     race on it and may report wrong counts.
+ */
+#define NM_NOALLOC_SCRATCH_BYTES 256
+#define NM_PACK_NOALLOC_MAX_GROUPS 4294967295LL
+nm_status nm_pack_noalloc(const void *W, const uint8_t *mask, int64_t rows, int64_t K,
+                          int N, int M, void *values, uint32_t *masks, nm_stream_t stream);
+
+/*
  * Expand a packed matrix back to dense fp16 [rows][K] (dropped positions
  * become +0.0).  A test and debugging aid; asynchronous on `stream`.
  * W_out: device, 2-byte aligned, rows*K*2 bytes, overwritten.

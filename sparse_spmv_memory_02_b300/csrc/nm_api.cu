@@ -96,6 +96,11 @@ nm_status check_matrix(const nm_matrix *A)
 
 }  // namespace
 
+void nm::set_last_error(const char *msg)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s", msg);
+}
+
 extern "C" {
 
 int nm_version(void) { return NM_VERSION; }

@@ -45,4 +45,7 @@ cudaError_t launch_unpack(const uint16_t *values, const uint32_t *masks, int64_t
 // Cached device attributes of the current device.
 int sm_count();
 
+// Set the calling thread's message returned by nm_last_error().
+void set_last_error(const char *msg);
+
 }  // namespace nm
