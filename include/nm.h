@@ -156,6 +156,13 @@ nm_status nm_unpack(const nm_matrix *A, void *W_out, nm_stream_t stream);
  * Asynchronous: never synchronises, allocates nothing, and may be captured
  * in a CUDA graph.  Results for a matrix with invalid groups are unspecified
  * (never out of bounds).
+ * Overlap with the preceding kernel: the call is launched with programmatic
+ * dependent launch, so it may start streaming A's packed arrays while the
+ * kernel before it in `stream` is still running; it reads x and writes y only
+ * after that kernel has completed.  A's arrays must therefore not be written
+ * by the kernel immediately before the call (nm_pack, which synchronises,
+ * and copies are fine).  NM_BULK_TUNE=pdl=0 in the environment turns this
+ * off.
  */
 nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
                   nm_stream_t stream);
@@ -171,6 +178,20 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
 nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
                           void *y, int64_t ldy, int batch, nm_dtype y_type,
                           nm_stream_t stream);
+
+/*
+ * Read the device error word of the calling thread's current device into
+ * *flags and, if `clear` is nonzero, reset it to zero.  A kernel of this
+ * library sets NM_DEVERR_PIPE_TIMEOUT when one of its internal pipeline
+ * waits (shared-memory barriers between its copy and compute warps) has not
+ * completed within about two seconds; the kernel then stops waiting, ends,
+ * and the y it wrote is unspecified.  This never happens in a correct run;
+ * the word lets a caller check for it after the fact.  Synchronises
+ * `stream` (so it cannot be captured in a CUDA graph).
+ * Errors: NM_ERR_INVALID_ARG (flags NULL, capturing stream), NM_ERR_CUDA.
+ */
+#define NM_DEVERR_PIPE_TIMEOUT 1u
+nm_status nm_device_errors(uint32_t *flags, int clear, nm_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *nm_status_str(nm_status status);

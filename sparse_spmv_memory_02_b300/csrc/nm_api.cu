@@ -2,6 +2,7 @@
 // host, then one kernel launch.  No exception crosses this file's functions.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -17,6 +18,20 @@ cudaError_t launch_fast_1_8(const SpmvProblem &, cudaStream_t);
 cudaError_t launch_fast_2_8(const SpmvProblem &, cudaStream_t);
 cudaError_t launch_fast_4_8(const SpmvProblem &, cudaStream_t);
 cudaError_t launch_fast_8_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_1_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_2_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_4_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_1_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_2_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_4_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_bulk_8_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_1_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_2_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_4_4(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_1_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_2_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_4_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_8_8(const SpmvProblem &, cudaStream_t);
 
 bool fast_path_applies(int N, int M, int64_t K)
 {
@@ -24,6 +39,39 @@ bool fast_path_applies(int N, int M, int64_t K)
     if (N < 1 || N > M || 8 % N != 0) return false;
     const int64_t ck = 8 * M / N;  // positions covered by one 16-byte value chunk
     return K > 0 && K % ck == 0 && K / ck <= INT_MAX / 2;
+}
+
+bool bulk_path_applies(int N, int M, int64_t K)
+{
+    return fast_path_applies(N, M, K) && K % 128 == 0;
+}
+
+cudaError_t launch_rows(const SpmvProblem &p, cudaStream_t s)
+{
+    switch (p.M * 16 + p.N) {
+    case 4 * 16 + 1: return launch_rows_1_4(p, s);
+    case 4 * 16 + 2: return launch_rows_2_4(p, s);
+    case 4 * 16 + 4: return launch_rows_4_4(p, s);
+    case 8 * 16 + 1: return launch_rows_1_8(p, s);
+    case 8 * 16 + 2: return launch_rows_2_8(p, s);
+    case 8 * 16 + 4: return launch_rows_4_8(p, s);
+    case 8 * 16 + 8: return launch_rows_8_8(p, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+cudaError_t launch_bulk(const SpmvProblem &p, cudaStream_t s)
+{
+    switch (p.M * 16 + p.N) {
+    case 4 * 16 + 1: return launch_bulk_1_4(p, s);
+    case 4 * 16 + 2: return launch_bulk_2_4(p, s);
+    case 4 * 16 + 4: return launch_bulk_4_4(p, s);
+    case 8 * 16 + 1: return launch_bulk_1_8(p, s);
+    case 8 * 16 + 2: return launch_bulk_2_8(p, s);
+    case 8 * 16 + 4: return launch_bulk_4_8(p, s);
+    case 8 * 16 + 8: return launch_bulk_8_8(p, s);
+    default: return cudaErrorNotSupported;
+    }
 }
 
 cudaError_t launch_fast(const SpmvProblem &p, cudaStream_t s)
@@ -44,6 +92,31 @@ cudaError_t launch_fast(const SpmvProblem &p, cudaStream_t s)
 namespace {
 
 thread_local char g_last_error[512];
+
+// The device error word: kernels set bits in it when an internal pipeline
+// wait gives up (see nm_device_errors).  Its device address is looked up
+// once per device.
+__device__ unsigned int g_device_error;
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned int *> g_error_ptr[kMaxDevices];
+
+cudaError_t device_error_word(unsigned int **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned int *p = g_error_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *v = nullptr;
+        e = cudaGetSymbolAddress(&v, g_device_error);
+        if (e != cudaSuccess) return e;
+        p = static_cast<unsigned int *>(v);
+        g_error_ptr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return cudaSuccess;
+}
 
 nm_status fail(nm_status st, const char *fmt, ...)
 {
@@ -234,9 +307,38 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx, void *
     p.ldy = ldy;
     p.batch = batch;
     p.y_f32 = y_type == NM_F32;
-    cudaError_t e = nm::fast_path_applies(p.N, p.M, p.K) ? nm::launch_fast(p, s)
-                                                         : nm::launch_generic(p, s);
+    cudaError_t e = device_error_word(&p.err);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: device error word");
+    e = cudaErrorNotSupported;
+    if (nm::bulk_path_applies(p.N, p.M, p.K)) {
+        e = nm::launch_rows(p, s);
+        if (e == cudaErrorNotSupported) e = nm::launch_bulk(p, s);
+    }
+    if (e == cudaErrorNotSupported)
+        e = nm::fast_path_applies(p.N, p.M, p.K) ? nm::launch_fast(p, s) : nm::launch_generic(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "nm_spmv launch");
+    return NM_OK;
+}
+
+nm_status nm_device_errors(uint32_t *flags, int clear, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    if (!flags) return fail(NM_ERR_INVALID_ARG, "flags is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_device_errors: cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(NM_ERR_INVALID_ARG, "nm_device_errors synchronises and cannot be captured");
+    unsigned int *d = nullptr;
+    e = device_error_word(&d);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_device_errors: device error word");
+    unsigned int h = 0;
+    e = cudaMemcpyAsync(&h, d, sizeof(h), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(d, 0, sizeof(unsigned int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_device_errors");
+    *flags = h;
     return NM_OK;
 }
 

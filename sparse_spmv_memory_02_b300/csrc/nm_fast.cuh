@@ -39,107 +39,177 @@
 namespace nm {
 
 // ---------------------------------------------------------------- patterns
-// Pattern<N, M>::dot(v, m, x, acc): add the products of one chunk's 8 kept
-// values `v` with x, where `m` holds the chunk's CK mask bits and `x` the
-// chunk's CK fp16 activations packed two per word (XR = CK/2 words).
+// Pattern<N, M> consumes one 16-byte chunk of kept values (8 fp16 = 8/N
+// groups spanning CK = 8*M/N positions along K) and its CK mask bits.
+//   decode(m) -> Sel: everything that depends on the mask alone (the byte
+//                permute selectors that gather the x lanes of the kept
+//                positions); done once per chunk and shared by all vectors.
+//   dot(v, sel, x, acc): acc + the products of the 8 values with the
+//                matching x lanes, x = the chunk's CK fp16 activations
+//                packed two per word (XR = CK/2 words).
+// Results for groups without exactly N set bits are unspecified; the mask
+// only ever feeds byte permutes and selects, never an address.
 
 template <int N, int M> struct Pattern;
 
-template <> struct Pattern<2, 4> {  // 4 groups of 4 per chunk, one value pair per group
+// 2:4 -- four groups per chunk, one value pair per group.  A valid nibble
+// has exactly two set bits, so its low three bits already identify it; two
+// 8-entry byte tables (held in immediates, indexed by byte permutes) map
+// those bits to the selector bytes of the first and second kept lane.
+template <> struct Pattern<2, 4> {
     static constexpr int CK = 16;
     using mask_t = uint16_t;
-    __device__ static __forceinline__ float dot(const uint4 &v, uint32_t m, const uint32_t *x,
+    struct Sel { uint32_t s[4]; };
+    __device__ static __forceinline__ Sel decode(uint32_t m)
+    {
+        const uint32_t idx = m & 0x7777u;
+        const uint32_t first = prmt(0x10321010u, 0x10321054u, idx);   // lane of the lower kept k
+        const uint32_t second = prmt(0x32767676u, 0x76545476u, idx);  // lane of the upper kept k
+        const uint32_t s01 = prmt(first, second, 0x5140u);
+        const uint32_t s23 = prmt(first, second, 0x7362u);
+        return Sel{{s01, s01 >> 16, s23, s23 >> 16}};
+    }
+    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const uint32_t nib = (m >> (4 * g)) & 0xFu;
-            const uint32_t xp = prmt(x[2 * g], x[2 * g + 1], sel_pair(ctz(nib), msb(nib)));
-            acc = fma_h2(vw[g], xp, acc);
-        }
-        return acc;
+        acc = fma_h2(v.x, prmt(x[0], x[1], sel.s[0]), acc);
+        acc = fma_h2(v.y, prmt(x[2], x[3], sel.s[1]), acc);
+        acc = fma_h2(v.z, prmt(x[4], x[5], sel.s[2]), acc);
+        return fma_h2(v.w, prmt(x[6], x[7], sel.s[3]), acc);
     }
 };
 
-template <> struct Pattern<4, 8> {  // 2 groups of 8 per chunk, two value pairs per group
-    static constexpr int CK = 16;
-    using mask_t = uint16_t;
-    __device__ static __forceinline__ float dot(const uint4 &v, uint32_t m, const uint32_t *x,
-                                                float acc)
-    {
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            const uint32_t b0 = (m >> (8 * g)) & 0xFFu;
-            const uint32_t b1 = b0 & (b0 - 1u);
-            const uint32_t b2 = b1 & (b1 - 1u);
-            const uint32_t p0 = ctz(b0), p1 = ctz(b1), p2 = ctz(b2), p3 = msb(b0);
-            const uint32_t *xg = x + 4 * g;
-            acc = fma_h2(vw[2 * g], gather_pair8(xg[0], xg[1], xg[2], xg[3], p0, p1), acc);
-            acc = fma_h2(vw[2 * g + 1], gather_pair8(xg[0], xg[1], xg[2], xg[3], p2, p3), acc);
-        }
-        return acc;
-    }
-};
-
-template <> struct Pattern<1, 4> {  // 8 groups of 4 per chunk; a value pair spans two groups
+// 1:4 -- eight groups per chunk; a value pair spans two groups.  A valid
+// nibble has one set bit and its low three bits identify it (8 -> 0).
+template <> struct Pattern<1, 4> {
     static constexpr int CK = 32;
     using mask_t = uint32_t;
-    __device__ static __forceinline__ float dot(const uint4 &v, uint32_t m, const uint32_t *x,
+    struct Sel { uint32_t s[4]; };
+    __device__ static __forceinline__ Sel decode(uint32_t m)
+    {
+        const uint32_t lo = prmt(0x10321076u, 0x10101054u, m & 0x7777u);
+        const uint32_t hi = prmt(0x10321076u, 0x10101054u, (m >> 16) & 0x7777u);
+        return Sel{{lo, lo >> 16, hi, hi >> 16}};
+    }
+    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint32_t pa = ctz((m >> (8 * q)) & 0xFu);
-            const uint32_t pb = ctz((m >> (8 * q + 4)) & 0xFu);
-            const uint32_t ra = (pa & 2u) ? x[4 * q + 1] : x[4 * q];
-            const uint32_t rb = (pb & 2u) ? x[4 * q + 3] : x[4 * q + 2];
-            const uint32_t s = 0x5410u + 0x22u * (pa & 1u) + 0x2200u * (pb & 1u);
-            acc = fma_h2(vw[q], prmt(ra, rb, s), acc);
+            // low half: lane of group 2q; high half: lane of group 2q+1
+            const uint32_t a = prmt(x[4 * q], x[4 * q + 1], sel.s[q]);
+            const uint32_t b = prmt(x[4 * q + 2], x[4 * q + 3], sel.s[q]);
+            acc = fma_h2(vw[q], prmt(a, b, 0x7610u), acc);
         }
         return acc;
     }
 };
 
-template <> struct Pattern<2, 8> {  // 4 groups of 8 per chunk, one value pair per group
+// Selector pair that gathers fp16 lanes pa and pb (0..7) of four words with
+// gather8(): a permute of words 0-1 and one of words 2-3 by the lanes'
+// positions within a half, then a permute picking the half each lives in.
+struct Pair8 { uint32_t s, pick; };
+__device__ __forceinline__ Pair8 pair8(uint32_t pa, uint32_t pb)
+{
+    return Pair8{sel_pair(pa & 3u, pb & 3u),
+                 ((pa & 4u) ? 0x54u : 0x10u) | ((pb & 4u) ? 0x7600u : 0x3200u)};
+}
+__device__ __forceinline__ uint32_t gather8(const uint32_t *xg, const Pair8 &p)
+{
+    return prmt(prmt(xg[0], xg[1], p.s), prmt(xg[2], xg[3], p.s), p.pick);
+}
+// Position of the lowest / highest set bit of a nonzero byte (one
+// find-leading-one each; the lowest set bit is isolated with b & -b).
+__device__ __forceinline__ uint32_t lowest(uint32_t b) { return msb(b & (0u - b)); }
+
+// 2:8 -- four groups of 8 per chunk, one value pair per group.
+template <> struct Pattern<2, 8> {
     static constexpr int CK = 32;
     using mask_t = uint32_t;
-    __device__ static __forceinline__ float dot(const uint4 &v, uint32_t m, const uint32_t *x,
+    struct Sel { Pair8 p[4]; };
+    __device__ static __forceinline__ Sel decode(uint32_t m)
+    {
+        Sel s;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t b = (m >> (8 * g)) & 0xFFu;
+            s.p[g] = pair8(lowest(b), msb(b));
+        }
+        return s;
+    }
+    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const uint32_t byte = (m >> (8 * g)) & 0xFFu;
-            const uint32_t *xg = x + 4 * g;
-            acc = fma_h2(vw[g], gather_pair8(xg[0], xg[1], xg[2], xg[3], ctz(byte), msb(byte)),
-                         acc);
-        }
+        for (int g = 0; g < 4; ++g) acc = fma_h2(vw[g], gather8(x + 4 * g, sel.p[g]), acc);
         return acc;
     }
 };
 
-template <> struct Pattern<1, 8> {  // 8 groups of 8 per chunk; a value pair spans two groups
-    static constexpr int CK = 64;
-    using mask_t = uint64_t;
-    __device__ static __forceinline__ float dot(const uint4 &v, uint64_t m, const uint32_t *x,
+// 4:8 -- two groups of 8 per chunk, two value pairs per group: the two
+// lowest and the two highest kept positions.
+template <> struct Pattern<4, 8> {
+    static constexpr int CK = 16;
+    using mask_t = uint16_t;
+    struct Sel { Pair8 p[4]; };
+    __device__ static __forceinline__ Sel decode(uint32_t m)
+    {
+        Sel s;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const uint32_t b = (m >> (8 * g)) & 0xFFu;
+            const uint32_t p0 = lowest(b);
+            const uint32_t p1 = lowest(b & (b - 1u));
+            const uint32_t p3 = msb(b);
+            const uint32_t p2 = msb(b & ~(1u << p3));
+            s.p[2 * g] = pair8(p0, p1);
+            s.p[2 * g + 1] = pair8(p2, p3);
+        }
+        return s;
+    }
+    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
-        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        acc = fma_h2(v.x, gather8(x, sel.p[0]), acc);
+        acc = fma_h2(v.y, gather8(x, sel.p[1]), acc);
+        acc = fma_h2(v.z, gather8(x + 4, sel.p[2]), acc);
+        return fma_h2(v.w, gather8(x + 4, sel.p[3]), acc);
+    }
+};
+
+// 1:8 -- eight groups of 8 per chunk; a value pair spans two groups.  The
+// single set bit of a group is its highest.
+template <> struct Pattern<1, 8> {
+    static constexpr int CK = 64;
+    using mask_t = uint64_t;
+    struct Sel { uint32_t pa[4], pb[4]; };
+    __device__ static __forceinline__ Sel decode(uint64_t m)
+    {
+        Sel s;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const uint32_t bits = static_cast<uint32_t>(m >> (16 * q));
-            const uint32_t pa = ctz(bits & 0xFFu);
-            const uint32_t pb = ctz((bits >> 8) & 0xFFu);
+            s.pa[q] = msb(bits & 0xFFu);
+            s.pb[q] = msb((bits >> 8) & 0xFFu);
+        }
+        return s;
+    }
+    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
+                                                float acc)
+    {
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t pa = sel.pa[q], pb = sel.pb[q];
             const uint32_t *xa = x + 8 * q;      // group 2q: 8 fp16 in 4 words
             const uint32_t *xb = x + 8 * q + 4;  // group 2q+1
-            const uint32_t ia = pa >> 1, ib = pb >> 1;
+            const uint32_t ia = (pa >> 1) & 3u, ib = (pb >> 1) & 3u;
             const uint32_t ra = (ia & 2u) ? ((ia & 1u) ? xa[3] : xa[2]) : ((ia & 1u) ? xa[1] : xa[0]);
             const uint32_t rb = (ib & 2u) ? ((ib & 1u) ? xb[3] : xb[2]) : ((ib & 1u) ? xb[1] : xb[0]);
-            const uint32_t s = 0x5410u + 0x22u * (pa & 1u) + 0x2200u * (pb & 1u);
-            acc = fma_h2(vw[q], prmt(ra, rb, s), acc);
+            const uint32_t sl = 0x5410u + 0x22u * (pa & 1u) + 0x2200u * (pb & 1u);
+            acc = fma_h2(vw[q], prmt(ra, rb, sl), acc);
         }
         return acc;
     }
@@ -148,7 +218,9 @@ template <> struct Pattern<1, 8> {  // 8 groups of 8 per chunk; a value pair spa
 template <int M> struct DensePattern {  // N == M: every position kept, mask not consulted
     static constexpr int CK = 8;
     using mask_t = uint8_t;
-    __device__ static __forceinline__ float dot(const uint4 &v, uint32_t, const uint32_t *x,
+    struct Sel {};
+    __device__ static __forceinline__ Sel decode(uint32_t) { return Sel{}; }
+    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &, const uint32_t *x,
                                                 float acc)
     {
         acc = fma_h2(v.x, x[0], acc);
@@ -278,10 +350,12 @@ nm_spmv_fast_kernel(const FastArgs a)
 #pragma unroll
             for (int i = 0; i < R; ++i)
 #pragma unroll
-                for (int j = 0; j < CPL; ++j)
+                for (int j = 0; j < CPL; ++j) {
+                    const typename P::Sel sel = P::decode(m[i][j]);
 #pragma unroll
                     for (int b = 0; b < B; ++b)
-                        acc[i * B + b] = P::dot(v[i][j], m[i][j], xr[j][b], acc[i * B + b]);
+                        acc[i * B + b] = P::dot(v[i][j], sel, xr[j][b], acc[i * B + b]);
+                }
 
             warp_reduce_scatter<V>(acc, lane);
             constexpr int SH = 5 - log2i<V>();

@@ -23,6 +23,7 @@ struct SpmvProblem {
     int64_t ldy;
     int batch;
     bool y_f32;
+    unsigned int *err;  // device error word (see nm_device_errors)
 };
 
 // Vectorised kernel: 8 % N == 0 and K a multiple of the k-span of one
@@ -30,6 +31,15 @@ struct SpmvProblem {
 // per K tile sweep (any K is handled by tiling K inside a block).
 bool fast_path_applies(int N, int M, int64_t K);
 cudaError_t launch_fast(const SpmvProblem &p, cudaStream_t s);
+
+// Bulk-staged kernels (the main path): a fast pattern and K a multiple of
+// 128, so that every row's value and mask segments are 16-byte multiples.
+// launch_rows (row-per-warp, batch <= 2) is tried first, then launch_bulk
+// (chunk columns per thread, any batch).  Both return cudaErrorNotSupported,
+// having launched nothing, if no tiling fits in shared memory.
+bool bulk_path_applies(int N, int M, int64_t K);
+cudaError_t launch_rows(const SpmvProblem &p, cudaStream_t s);  // batch <= 2
+cudaError_t launch_bulk(const SpmvProblem &p, cudaStream_t s);
 
 // Scalar kernel for every valid pattern and K (patterns like 3:4, or K not
 // a multiple of the chunk span).
@@ -44,6 +54,7 @@ cudaError_t launch_unpack(const uint16_t *values, const uint32_t *masks, int64_t
 
 // Cached device attributes of the current device.
 int sm_count();
+int max_dynamic_smem();
 
 // Set the calling thread's message returned by nm_last_error().
 void set_last_error(const char *msg);

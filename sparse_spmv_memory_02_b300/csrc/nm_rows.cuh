@@ -1,0 +1,357 @@
+// N:M SpMV for one or two vectors: every warp owns whole rows and streams
+// its own weights into shared memory with bulk (TMA) copies; x is held once
+// per CTA in shared memory.  The main kernel of libnm at batch 1.
+//
+// The operation is the N:M sparse matrix-vector product with bitmask
+// indexing and fixed-step traversal of "SparseDecoding: Decoding-Aware
+// Pruning for Accurate and Efficient LLM Inference" (Abstract); at batch 1
+// it is the whole decode-step cost of an N:M-pruned linear layer.  Each kept
+// value and mask bit is read from HBM once, so the kernel's job is to keep
+// enough bytes in flight with as few instructions per byte as possible.
+//
+// Work split.  Rows are split evenly over one CTA per SM.  A CTA's rows form
+// row tiles of R rows; with K split into K tiles (usually one), a task is
+// one row tile x one K tile, and task (kt, rt) belongs to warp rt % W.
+//
+// Self-feeding warps.  Warp w owns SW shared-memory slots.  Its lane 0
+// issues the bulk copies of w's own next SW tasks (the R rows' value
+// segments and mask segments; with a single K tile the R rows are one
+// contiguous byte range of each array -- a packed row is exactly K/M*N
+// values and K/32 mask words -- so a task is two copies), each completing on
+// the slot's mbarrier.  After the warp has read a slot it immediately issues
+// its task SW ahead into it.  Every warp is thus its own pipeline with SW-1
+// tasks in flight: bulk copies issued by one warp complete at a limited rate
+// per warp on this GPU, and W independent issuers per SM are what reach HBM
+// bandwidth.  There is no producer warp, no "empty" barrier and no
+// synchronisation between warps other than one named barrier per K tile.
+// A warp waits on every phase of its own slots in order, so a parity wait
+// can never mistake an older phase for the one it wants.
+//
+// Per task, lane l walks the chunk columns l, l+32, ... of the K tile: it
+// loads the column's x units from shared memory once and uses them for all R
+// rows (each a 16-byte value chunk plus its mask bits, decoded by byte
+// permutes in Pattern<N, M>), accumulating in fp32; the warp reduces its R*B
+// sums with a reduce-scatter butterfly and one lane per sum rounds it into y
+// (or adds it to the row's carry when the row spans several K tiles; a row's
+// tiles always go to the same warp).
+//
+// Programmatic dependent launch: the first SW tasks of every warp are issued
+// before griddepcontrol.wait -- the packed weights are read-only input that
+// no kernel of this library writes -- so one call's weight stream starts
+// under the tail of the previous call; x is read and y written only after
+// the wait.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "nm_bulk.cuh"  // Pattern<N, M>, pipeline primitives, tuning
+
+namespace nm {
+
+struct RowsArgs {
+    const uint8_t *values;  // [rows][vrow_bytes]
+    const uint8_t *masks;   // [rows][mrow_bytes]
+    const __half *x;        // [B][ldx]
+    void *y;                // [B][ldy]
+    unsigned int *err;      // device error word
+    int64_t ldx, ldy, vrow_bytes, mrow_bytes;
+    int rows, chunks;       // 16-byte value chunks per row
+    int tile_chunks;        // chunks per K tile
+    int ktiles;
+    int SW;                 // slots per warp
+    int seg_v, seg_m;       // shared bytes of one row's value / mask segment
+    int stage_bytes;        // R * (seg_v + seg_m)
+    int xbuf_bytes;         // one x tile buffer: B * XV * tile_chunks * 16
+    int off_x, off_bar, off_carry;
+    int row_base, row_extra;  // CTA c owns row_base rows (+1 if c < row_extra)
+    int y_f32;
+};
+
+constexpr int kRowsMaxWarps = 16;
+
+// Where task j of warp w lives: K tile and row tile.
+struct RowsTask {
+    int kt, rt;
+};
+__device__ __forceinline__ RowsTask rows_task(int j, int w, int W, int per_kt)
+{
+    const int kt = j / per_kt;
+    return RowsTask{kt, w + (j - kt * per_kt) * W};
+}
+
+template <int R, int MB>
+__device__ __forceinline__ void rows_issue(const RowsArgs &a, uint8_t *st, uint64_t *bar, int kt,
+                                           int i0, int nr, int r_begin, uint64_t pol)
+{
+    const int c0 = kt * a.tile_chunks;
+    const int nc = min(a.tile_chunks, a.chunks - c0);
+    const uint32_t vb = static_cast<uint32_t>(nc) * 16u;
+    const uint32_t mb = static_cast<uint32_t>(nc) * MB;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * (vb + mb));
+    const int64_t row0 = r_begin + i0;
+    if (a.ktiles == 1) {
+        // whole rows: seg_v == vrow_bytes and seg_m == mrow_bytes, so the
+        // rows are one contiguous range of each array, in the slot's layout
+        bulk_g2s(st, a.values + row0 * a.vrow_bytes, static_cast<uint32_t>(nr) * vb, bar, pol);
+        bulk_g2s(st + R * a.seg_v, a.masks + row0 * a.mrow_bytes, static_cast<uint32_t>(nr) * mb,
+                 bar, pol);
+    } else {
+        for (int i = 0; i < nr; ++i) {
+            const int64_t row = row0 + i;
+            bulk_g2s(st + i * a.seg_v, a.values + row * a.vrow_bytes + c0 * 16LL, vb, bar, pol);
+            bulk_g2s(st + R * a.seg_v + i * a.seg_m,
+                     a.masks + row * a.mrow_bytes + static_cast<int64_t>(c0) * MB, mb, bar, pol);
+        }
+    }
+}
+
+template <int N, int M, int B, int R>
+__global__ void __launch_bounds__(32 * kRowsMaxWarps, 1)
+nm_spmv_rows_kernel(const RowsArgs a)
+{
+    using P = Pattern<N, M>;
+    using mask_t = typename P::mask_t;
+    constexpr int CK = P::CK;
+    constexpr int XR = CK / 2;  // x words per chunk and vector
+    constexpr int XV = CK / 8;  // 16-byte x units per chunk and vector
+    constexpr int MB = CK / 8;  // mask bytes per chunk
+    constexpr int V = pow2_ceil(R * B);
+    constexpr int SH = 5 - log2i<V>();
+
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    const int W = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t *ring = rows_smem;                                             // [W][SW] slots
+    uint8_t *xbuf = rows_smem + a.off_x;                                   // [<=2][B][XV][tile]
+    uint64_t *full = reinterpret_cast<uint64_t *>(rows_smem + a.off_bar);  // [W][SW]
+    float *carry = reinterpret_cast<float *>(rows_smem + a.off_carry);     // [rows of CTA][B]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < W * a.SW; ++s) mbar_init(&full[s], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    const int cta = blockIdx.x;
+    const int r_begin = cta * a.row_base + min(cta, a.row_extra);
+    const int r_count = a.row_base + (cta < a.row_extra ? 1 : 0);
+    const int nrt = (r_count + R - 1) / R;                         // row tiles of the CTA
+    const int per_kt = nrt > warp ? (nrt - warp + W - 1) / W : 0;  // this warp's tiles per K tile
+    const int ntask = per_kt * a.ktiles;
+    uint8_t *my_ring = ring + static_cast<size_t>(warp) * a.SW * a.stage_bytes;
+    uint64_t *my_full = full + warp * a.SW;
+    const uint64_t pol = l2_evict_first_policy();
+
+    // Prefetch this warp's first SW tasks (weights only: no dependence on
+    // the previous kernel).
+    int issued = 0;
+    if (lane == 0) {
+        for (; issued < a.SW && issued < ntask; ++issued) {
+            const RowsTask t = rows_task(issued, warp, W, per_kt);
+            rows_issue<R, MB>(a, my_ring + static_cast<size_t>(issued) * a.stage_bytes,
+                              &my_full[issued], t.kt, t.rt * R, min(R, r_count - t.rt * R),
+                              r_begin, pol);
+        }
+    }
+
+    pdl_wait();  // x may be the previous kernel's output; y may still be read by it
+
+    bool failed = false;
+    int j = 0;  // next task of this warp
+    for (int kt = 0; kt < a.ktiles; ++kt) {
+        const int c0 = kt * a.tile_chunks;
+        const int nc = min(a.tile_chunks, a.chunks - c0);
+        uint8_t *xs = xbuf + (kt & 1) * a.xbuf_bytes;
+        // x tile -> shared memory, unit-major: unit u of chunk column c of
+        // vector b at ((b * XV + u) * tile_chunks + c) * 16, so that a warp
+        // reading one unit of 32 consecutive columns reads 512 contiguous
+        // bytes.  The buffer written here was last read in K tile kt-2, and
+        // every warp has passed the barrier of tile kt-1 since.
+        for (int e = threadIdx.x; e < B * XV * nc; e += blockDim.x) {
+            const int b = e / (XV * nc);
+            const int r = e - b * (XV * nc);
+            const int c = r / XV, u = r - (r / XV) * XV;
+            const uint4 t = ld_cg_v4(a.x + b * a.ldx + static_cast<int64_t>(c0 + c) * CK + 8 * u);
+            *reinterpret_cast<uint4 *>(xs + ((b * XV + u) * a.tile_chunks + c) * 16) = t;
+        }
+        named_barrier_sync(1, blockDim.x);
+
+        for (int n = 0; n < per_kt; ++n, ++j) {
+            const int slot = j % a.SW;
+            const int rt = warp + n * W;
+            const int i0 = rt * R;
+            const int nr = min(R, r_count - i0);
+            if (!failed && !mbar_wait(&my_full[slot], (j / a.SW) & 1)) {
+                failed = true;  // give up waiting; y is garbage, the error word says so
+                atomicOr(a.err, kDevErrPipeTimeout);
+            }
+            uint8_t *sv = my_ring + static_cast<size_t>(slot) * a.stage_bytes;
+            const uint8_t *sm = sv + R * a.seg_v;
+
+            float acc[V];
+#pragma unroll
+            for (int t = 0; t < V; ++t) acc[t] = 0.f;
+#pragma unroll 2
+            for (int c = lane; c < nc; c += 32) {
+                uint32_t xw[B][XR];
+#pragma unroll
+                for (int b = 0; b < B; ++b)
+#pragma unroll
+                    for (int u = 0; u < XV; ++u) {
+                        const uint4 t = *reinterpret_cast<const uint4 *>(
+                            xs + ((b * XV + u) * a.tile_chunks + c) * 16);
+                        xw[b][4 * u + 0] = t.x;
+                        xw[b][4 * u + 1] = t.y;
+                        xw[b][4 * u + 2] = t.z;
+                        xw[b][4 * u + 3] = t.w;
+                    }
+#pragma unroll
+                for (int i = 0; i < R; ++i) {
+                    if (i < nr) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
+                        const mask_t m = *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
+                        const typename P::Sel sel = P::decode(m);
+#pragma unroll
+                        for (int b = 0; b < B; ++b)
+                            acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
+                    }
+                }
+            }
+            // Every lane has read the slot: refill it with this warp's task
+            // SW ahead (generic-proxy reads, then async-proxy writes of the
+            // same bytes: fence between them).
+            __syncwarp();
+            if (lane == 0 && issued < ntask && !failed) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const RowsTask t = rows_task(issued, warp, W, per_kt);
+                rows_issue<R, MB>(a, sv, &my_full[slot], t.kt, t.rt * R,
+                                  min(R, r_count - t.rt * R), r_begin, pol);
+                ++issued;
+            }
+
+            warp_reduce_scatter<V>(acc, lane);
+            const int idx = lane >> SH;
+            if ((lane & ((1 << SH) - 1)) == 0 && idx < nr * B) {
+                const int i = idx / B, b = idx - (idx / B) * B;
+                float tot = acc[0];
+                if (a.ktiles > 1) {
+                    float *cp = carry + (i0 + i) * B + b;
+                    if (kt > 0) tot += *cp;
+                    *cp = tot;
+                }
+                if (kt == a.ktiles - 1)
+                    store_y(a.y, b * a.ldy + r_begin + i0 + i, tot, a.y_f32 != 0);
+            }
+        }
+    }
+    // After a timeout, copies this warp issued may still be landing in its
+    // slots: wait for them (again with a limit) before the CTA can exit.
+    if (failed && lane == 0)
+        for (int p = j; p < issued; ++p)
+            if (!mbar_wait(&my_full[p % a.SW], (p / a.SW) & 1)) break;
+}
+
+// ---------------------------------------------------------------- host side
+
+struct RowsPlan {
+    int W, R, ktiles, tile_chunks, SW, grid;
+    int seg_v, seg_m, stage_bytes, xbuf_bytes, off_x, off_bar, off_carry;
+    size_t smem;
+};
+
+// Chooses rows per task, K tile, warps and slots per warp for a shape;
+// false if nothing fits in shared memory (the caller then takes another
+// kernel).
+bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, RowsPlan *out);
+
+template <int N, int M, int B, int R>
+cudaError_t launch_rows_instance(const SpmvProblem &p, const RowsPlan &pl, cudaStream_t s)
+{
+    auto kernel = nm_spmv_rows_kernel<N, M, B, R>;
+    static std::atomic<int> smem_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int need = static_cast<int>(pl.smem);
+    if (dev < 0 || dev >= 64 || need > smem_set[dev].load(std::memory_order_relaxed)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) {
+            int cur = smem_set[dev].load(std::memory_order_relaxed);
+            while (need > cur && !smem_set[dev].compare_exchange_weak(cur, need)) {
+            }
+        }
+    }
+    using P = Pattern<N, M>;
+    RowsArgs a;
+    a.values = static_cast<const uint8_t *>(p.values);
+    a.masks = reinterpret_cast<const uint8_t *>(p.masks);
+    a.x = static_cast<const __half *>(p.x);
+    a.y = p.y;
+    a.err = p.err;
+    a.ldx = p.ldx;
+    a.ldy = p.ldy;
+    a.vrow_bytes = p.K / P::CK * 16;
+    a.mrow_bytes = ((p.K + 31) / 32) * 4;
+    a.rows = static_cast<int>(p.rows);
+    a.chunks = static_cast<int>(p.K / P::CK);
+    a.tile_chunks = pl.tile_chunks;
+    a.ktiles = pl.ktiles;
+    a.SW = pl.SW;
+    a.seg_v = pl.seg_v;
+    a.seg_m = pl.seg_m;
+    a.stage_bytes = pl.stage_bytes;
+    a.xbuf_bytes = pl.xbuf_bytes;
+    a.off_x = pl.off_x;
+    a.off_bar = pl.off_bar;
+    a.off_carry = pl.off_carry;
+    a.row_base = a.rows / pl.grid;
+    a.row_extra = a.rows % pl.grid;
+    a.y_f32 = p.y_f32 ? 1 : 0;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid);
+    cfg.blockDim = dim3(32 * pl.W);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = bulk_tuning().pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+template <int N, int M, int B>
+cudaError_t launch_rows_b(const SpmvProblem &p, const RowsPlan &pl, cudaStream_t s)
+{
+    switch (pl.R) {
+    case 1: return launch_rows_instance<N, M, B, 1>(p, pl, s);
+    case 2: return launch_rows_instance<N, M, B, 2>(p, pl, s);
+    case 4: return launch_rows_instance<N, M, B, 4>(p, pl, s);
+    default: return cudaErrorNotSupported;
+    }
+}
+
+// Batch 1 and 2 only; cudaErrorNotSupported (nothing launched) otherwise or
+// when no plan fits.
+template <int N, int M>
+cudaError_t launch_rows_pattern(const SpmvProblem &p, cudaStream_t s)
+{
+    using P = Pattern<N, M>;
+    if (p.batch > 2) return cudaErrorNotSupported;
+    const int nsm = sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
+    const int max_smem = max_dynamic_smem();
+    if (max_smem <= 0) return cudaErrorInvalidDevice;
+    RowsPlan pl;
+    if (!rows_plan(p.rows, static_cast<int>(p.K / P::CK), P::CK, p.batch, nsm, max_smem, &pl))
+        return cudaErrorNotSupported;
+    return p.batch == 1 ? launch_rows_b<N, M, 1>(p, pl, s) : launch_rows_b<N, M, 2>(p, pl, s);
+}
+
+}  // namespace nm

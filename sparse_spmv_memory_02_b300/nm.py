@@ -7,7 +7,8 @@ shared library is missing the import of this module's functions fails
 loudly; there is no CPU fallback.
 
 The names mirror the C interface: nm_packed_sizes, nm_pack, nm_unpack,
-nm_spmv, nm_spmv_batched, nm_status_str, nm_last_error, nm_version.
+nm_spmv, nm_spmv_batched, nm_device_errors, nm_status_str, nm_last_error,
+nm_version.
 """
 from __future__ import annotations
 
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.nm_last_error.restype = ctypes.c_char_p
             L.nm_version.argtypes = []
             L.nm_version.restype = ctypes.c_int
+            L.nm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
+            L.nm_device_errors.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -89,6 +92,17 @@ def nm_last_error() -> str:
 
 def nm_version() -> int:
     return lib().nm_version()
+
+
+NM_DEVERR_PIPE_TIMEOUT = 1
+
+
+def nm_device_errors(clear: bool = True, stream=None) -> int:
+    """The device error word of the current device (0 after a correct run);
+    synchronises the stream, then clears the word if ``clear``."""
+    flags = ctypes.c_uint32(0)
+    _check(lib().nm_device_errors(ctypes.byref(flags), 1 if clear else 0, _stream(stream)))
+    return flags.value
 
 
 def _check(status: int):

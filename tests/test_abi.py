@@ -28,7 +28,13 @@ def declared_functions():
 
 def test_header_declares_the_interface():
     assert {"nm_packed_sizes", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_batched",
-            "nm_status_str", "nm_last_error", "nm_version"} <= set(declared_functions())
+            "nm_device_errors", "nm_status_str", "nm_last_error",
+            "nm_version"} <= set(declared_functions())
+
+
+def test_device_errors_rejects_null_on_the_host():
+    assert nm.lib().nm_device_errors(None, 0, None) == nm.NM_ERR_INVALID_ARG
+    assert "NULL" in nm.nm_last_error()
 
 
 def test_library_exports_every_declared_symbol():

@@ -1,0 +1,177 @@
+"""GPU parity of the bulk-staged SpMV kernels (the path every pattern with
+8 % N == 0 and K a multiple of 128 takes: the row-per-warp kernel at batch 1
+and 2, the chunk-column kernel at larger batches) against the CPU oracle.
+
+The shapes stress the kernel's schedule: fewer rows than CTAs, row counts
+that leave a ragged last stage, K tiles that do not divide the row, every
+batch size, and forced tunings (run in child processes, because the tuning
+is read once per process) that make rows span several K tiles, shrink the
+ring to two slots or one row per stage, and switch programmatic dependent
+launch off.  Consecutive dependent calls (the output of one call is the
+input of the next) check that a call reads x only after the previous kernel
+has written it.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import nm_synth
+import oracle
+from sparse_spmv_memory_02_b300 import nm
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FAST = [(2, 4), (4, 8), (1, 4), (2, 8), (4, 4), (1, 8), (8, 8)]
+
+
+def _np16(t):
+    return t.detach().cpu().numpy().view(np.uint16)
+
+
+def _case(rows, K, N, M, B, seed):
+    W = nm_synth.weights(rows, K, seed, DEV)
+    mask = nm_synth.topn_mask(W, N, M)
+    x = nm_synth.activations(K, B, seed + 500, True, DEV)
+    return W, mask, x
+
+
+def _check(y, W, mask, x):
+    yr, sr = oracle.spmv_dense(_np16(W), mask.cpu().numpy(), _np16(x))
+    yg = y.detach().double().cpu().numpy().reshape(yr.shape)
+    ok = oracle.within_tolerance(yg, yr, sr)
+    assert ok.all(), "%d/%d outside tolerance, first at %s" % (
+        (~ok).sum(), ok.size, np.argwhere(~ok)[:3].tolist())
+
+
+@pytest.mark.parametrize("N,M", FAST)
+@pytest.mark.parametrize("rows,K", [(1, 128), (7, 1024), (149, 4096), (300, 5120),
+                                    (600, 14336)])
+@pytest.mark.parametrize("B", [1, 2, 3, 5, 8])
+def test_bulk_matches_oracle(N, M, rows, K, B):
+    W, mask, x = _case(rows, K, N, M, B, seed=rows + K + 13 * N + M + 101 * B)
+    A = nm.nm_pack(W, mask, N, M)
+    ydt = torch.float32 if B % 2 else torch.float16
+    y = torch.full((B, rows), float("nan"), dtype=ydt, device=DEV)
+    if B == 1:
+        nm.nm_spmv(A, x[0], y[0])
+    else:
+        nm.nm_spmv_batched(A, x, y)
+    torch.cuda.synchronize()
+    _check(y, W, mask, x)
+
+
+def test_bulk_model_shapes_sampled_rows():
+    """Decode-layer shapes of the 8B block at batch 1, checked on a sample of
+    rows (the oracle computes those rows only)."""
+    g = np.random.default_rng(0)
+    for rows, K in [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]:
+        W, mask, x = _case(rows, K, 2, 4, 1, seed=rows + K)
+        A = nm.nm_pack(W, mask, 2, 4)
+        y = nm.nm_spmv(A, x[0], y_dtype=torch.float16)
+        torch.cuda.synchronize()
+        pick = np.sort(g.choice(rows, 256, replace=False))
+        idx = torch.from_numpy(pick).to(DEV)
+        _check(y[idx][None], W[idx], mask[idx], x)
+    assert nm.nm_device_errors() == 0
+
+
+def test_dependent_chain_reads_x_after_previous_call():
+    """y_i = A_i y_{i-1}: each call's x is the previous call's output.  The
+    chain run back to back must equal the same calls run one at a time with a
+    full synchronisation between them (the kernel is deterministic)."""
+    K = 4096
+    mats, bufs = [], [nm_synth.activations(K, 1, 7, True, DEV)[0] * 0.05]
+    for i in range(12):
+        W = nm_synth.weights(K, K, 900 + i, DEV, std=0.02)
+        mats.append(nm.nm_pack(W, nm_synth.topn_mask(W, 2, 4), 2, 4))
+        bufs.append(torch.full((K,), float("nan"), dtype=torch.float16, device=DEV))
+    torch.cuda.synchronize()
+    for i, A in enumerate(mats):
+        nm.nm_spmv(A, bufs[i], bufs[i + 1])
+    torch.cuda.synchronize()
+    chained = [b.clone() for b in bufs]
+    for i, A in enumerate(mats):
+        out = torch.full((K,), float("nan"), dtype=torch.float16, device=DEV)
+        nm.nm_spmv(A, chained[i], out)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), chained[i + 1].view(torch.int16)), i
+    assert torch.isfinite(chained[-1].float()).all()
+
+
+def test_dependent_chain_in_cuda_graph():
+    K, rows = 2048, 2048
+    W1 = nm_synth.weights(rows, K, 31, DEV)
+    W2 = nm_synth.weights(rows, rows, 32, DEV)
+    A1 = nm.nm_pack(W1, nm_synth.topn_mask(W1, 2, 4), 2, 4)
+    A2 = nm.nm_pack(W2, nm_synth.topn_mask(W2, 2, 4), 2, 4)
+    x = nm_synth.activations(K, 1, 33, True, DEV)[0]
+    h = torch.empty(rows, dtype=torch.float16, device=DEV)
+    y = torch.empty(rows, dtype=torch.float32, device=DEV)
+    nm.nm_spmv(A1, x, h)
+    nm.nm_spmv(A2, h, y)
+    torch.cuda.synchronize()
+    ref = y.clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            nm.nm_spmv(A1, x, h)
+            nm.nm_spmv(A2, h, y)
+    for _ in range(3):
+        h.fill_(float("nan"))
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref)
+
+
+def test_device_error_word_is_clear():
+    assert nm.nm_device_errors(clear=False) == 0
+    assert nm.nm_device_errors(clear=True) == 0
+
+
+_CHILD = r"""
+import json, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import nm_synth, oracle
+from sparse_spmv_memory_02_b300 import nm
+fails = []
+for (rows, K, N, M, B) in json.loads(sys.argv[2]):
+    W = nm_synth.weights(rows, K, rows + K, "cuda")
+    mask = nm_synth.topn_mask(W, N, M)
+    x = nm_synth.activations(K, B, rows + 3, True, "cuda")
+    A = nm.nm_pack(W, mask, N, M)
+    y = nm.nm_spmv_batched(A, x, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    Wn = W.cpu().numpy().view(np.uint16); xn = x.cpu().numpy().view(np.uint16)
+    yr, sr = oracle.spmv_dense(Wn, mask.cpu().numpy(), xn)
+    ok = oracle.within_tolerance(y.double().cpu().numpy(), yr, sr)
+    if not ok.all():
+        fails.append([rows, K, N, M, B, int((~ok).sum())])
+errs = nm.nm_device_errors()
+print(json.dumps({"fails": fails, "errors": errs}))
+"""
+
+
+@pytest.mark.parametrize("tune", ["warps=2,cpl=1,rows=0", "warps=3,cpl=2,R=1,rows=0",
+                                  "ring=4096,rows=0", "R=3,ring=20000,rows=0", "pdl=0",
+                                  "ctas=2,warps=4", "stage=1024,rows=0", "rows_R=1",
+                                  "rows_R=4,rows_warps=3", "rows_seg=1024", "rows_ring=4096",
+                                  "rows_warps=1,rows_seg=2048", "ctas=2"])
+def test_bulk_forced_tunings(tune):
+    cases = [(5, 4096, 2, 4, 1), (301, 8192, 2, 4, 2), (77, 14336, 4, 8, 1),
+             (150, 5120, 1, 4, 1), (64, 3072, 2, 8, 3), (33, 1024, 4, 4, 8)]
+    env = dict(os.environ, NM_BULK_TUNE=tune)
+    r = subprocess.run([sys.executable, "-c", _CHILD, ROOT, json.dumps(cases)], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    assert out["fails"] == [] and out["errors"] == 0, out
