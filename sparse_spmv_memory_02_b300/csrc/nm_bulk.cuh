@@ -251,17 +251,18 @@ struct BulkTuning {
     int pdl = 1;             // programmatic dependent launch
     // row-per-warp kernel (batch 1 and 2)
     int rows_kernel = 1;           // 0: never take it
-    int rows_warps = 0;            // warps per CTA (0: 8)
+    int rows_warps = 0;            // warps per CTA (0: 16)
     int rows_R = 0;                // rows per task (0: chosen)
-    int rows_task_bytes = 12288;   // largest task (rows x K tile) in bytes
-    int rows_ring_bytes = 163840;  // shared memory for the slots
+    int rows_task_bytes = 6144;    // largest task (rows x K tile) in bytes
+    int rows_ring_bytes = 200000;  // shared memory for the slots
     int rows_max_seg = 32768;      // longest row segment before K is tiled
+    int l2_prefetch_bytes = 0;     // weights warmed in L2 at CTA start (0: off)
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
-// rows_ring, rows_seg, rows (row-per-warp kernel), ctas, pdl (both); read
-// once per process.
+// rows_ring, rows_seg, rows (row-per-warp kernel), ctas, pdl, l2pf (both);
+// read once per process.
 const BulkTuning &bulk_tuning();
 
 struct BulkPlan {

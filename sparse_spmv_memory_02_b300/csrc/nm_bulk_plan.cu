@@ -42,6 +42,7 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "rows_ring") && v >= 4096) t.rows_ring_bytes = v;
         else if (!std::strcmp(tok, "rows_seg") && v >= 1024) t.rows_max_seg = v;
         else if (!std::strcmp(tok, "rows") && (v == 0 || v == 1)) t.rows_kernel = v;
+        else if (!std::strcmp(tok, "l2pf") && v >= 0) t.l2_prefetch_bytes = v / 16 * 16;
     }
     return t;
 }
@@ -150,7 +151,7 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, R
     const BulkTuning &t = bulk_tuning();
     if (!t.rows_kernel) return false;
     const int MB = CK / 8;  // mask bytes per chunk
-    const int W = t.rows_warps ? t.rows_warps : 8;
+    const int W = t.rows_warps ? t.rows_warps : 16;
     const int64_t row_bytes = static_cast<int64_t>(chunks) * (16 + MB);
     const int64_t x_bytes = static_cast<int64_t>(B) * chunks * CK * 2;
 

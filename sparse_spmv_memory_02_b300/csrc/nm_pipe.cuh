@@ -55,15 +55,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// The hint lets a thread whose phase is not complete sleep (up to the hint,
+// in ns) instead of spinning, which leaves issue slots to working warps.
+constexpr uint32_t kWaitSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kWaitSuspendHintNs)
         : "memory");
     return done != 0;
 }
@@ -76,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 7u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -98,6 +102,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
+}
+
+// Ask L2 to fetch `bytes` (a multiple of 16, 16-byte aligned address) from
+// HBM now; nothing waits for it.  Later reads of the range hit L2.
+__device__ __forceinline__ void prefetch_l2(const void *src_gmem, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes)
+                 : "memory");
 }
 
 // Programmatic dependent launch: let the next kernel in the stream start

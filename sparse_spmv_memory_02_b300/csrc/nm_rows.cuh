@@ -67,6 +67,7 @@ struct RowsArgs {
     int off_x, off_bar, off_carry;
     int row_base, row_extra;  // CTA c owns row_base rows (+1 if c < row_extra)
     int y_f32;
+    int pf_bytes;           // bytes of values (and matching masks) warmed in L2 per CTA
 };
 
 constexpr int kRowsMaxWarps = 16;
@@ -145,6 +146,25 @@ nm_spmv_rows_kernel(const RowsArgs a)
     uint8_t *my_ring = ring + static_cast<size_t>(warp) * a.SW * a.stage_bytes;
     uint64_t *my_full = full + warp * a.SW;
     const uint64_t pol = l2_evict_first_policy();
+
+    // Warm L2 with the start of this CTA's weights (values and masks of its
+    // rows are two contiguous ranges) while the previous kernel finishes and
+    // x becomes readable: up to pf_bytes in pieces of up to 32 KB, one piece
+    // per lane of the last warp, so the first tasks' copies below and the
+    // refills after them hit L2 instead of waiting on HBM.
+    if (warp == W - 1 && a.pf_bytes > 0) {
+        const int64_t vtot = static_cast<int64_t>(r_count) * a.vrow_bytes;
+        const int64_t mtot = static_cast<int64_t>(r_count) * a.mrow_bytes;
+        const int64_t vlen = min(vtot, static_cast<int64_t>(a.pf_bytes));
+        const int64_t mlen = min(mtot, vlen / (a.vrow_bytes / a.mrow_bytes)) / 16 * 16;
+        const uint8_t *vsrc = a.values + static_cast<int64_t>(r_begin) * a.vrow_bytes;
+        const uint8_t *msrc = a.masks + static_cast<int64_t>(r_begin) * a.mrow_bytes;
+        constexpr int64_t kPiece = 32768;
+        for (int64_t off = static_cast<int64_t>(lane) * kPiece; off < vlen; off += 32 * kPiece)
+            prefetch_l2(vsrc + off, static_cast<uint32_t>(min(kPiece, vlen - off)));
+        for (int64_t off = static_cast<int64_t>(lane) * kPiece; off < mlen; off += 32 * kPiece)
+            prefetch_l2(msrc + off, static_cast<uint32_t>(min(kPiece, mlen - off)));
+    }
 
     // Prefetch this warp's first SW tasks (weights only: no dependence on
     // the previous kernel).
@@ -312,6 +332,7 @@ cudaError_t launch_rows_instance(const SpmvProblem &p, const RowsPlan &pl, cudaS
     a.row_base = a.rows / pl.grid;
     a.row_extra = a.rows % pl.grid;
     a.y_f32 = p.y_f32 ? 1 : 0;
+    a.pf_bytes = bulk_tuning().l2_prefetch_bytes;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pl.grid);
