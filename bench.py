@@ -45,7 +45,7 @@ FALLBACK_HBM_GBS = 6400.0
 # the current kernel.
 TRAFFIC_PER_LAUNCH = {
     # profiles/nm_spmv_rows_llama31_8b_block_2of4_launches.md (21 launches)
-    ("llama31_8b_block", "2:4", 1): 35.095e6,
+    ("llama31_8b_block", "2:4", 1, "unfused"): 35.095e6,
 }
 
 
@@ -59,7 +59,10 @@ def parse_args(argv=None):
     p.add_argument("--pattern", default=None, help="N:M, default: the workload's first")
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--copies", type=int, default=3, help="rotating packed copies (L2 defeat)")
-    p.add_argument("--profile-steps", type=int, default=50, help="steps of the per-call pass")
+    p.add_argument("--profile-steps", type=int, default=50, help="calls per layer in the per-layer pass")
+    p.add_argument("--launch", choices=["fused", "unfused"], default="fused",
+                   help="fused: layers reading the same input (q/k/v, gate/up) share one "
+                        "nm_spmv_group launch; unfused: one nm_spmv launch per layer")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -190,11 +193,20 @@ def layer_list(wl):
 
 def build_workload(wl, N, M, batch, copies, device="cuda", keep_dense=False):
     """Generate, pack and replicate the layers of one step.  Returns a list of
-    dicts: name, rows, K, mats (packed copies), x, y, dense (optional)."""
+    dicts: name, rows, K, mats (packed copies), x, y, dense (optional).
+    Layers that read the same block input (q/k/v; gate/up) share one x
+    tensor."""
     from sparse_spmv_memory_02_b300 import nm
     layers = []
+    x_by_source = {}
     for li, layer in layer_list(wl):
         W, mask, x = nm_synth.layer_inputs(wl, li, layer, N, M, batch, device)
+        src = nm_synth.x_source(wl, li)
+        if src in x_by_source:
+            x = x_by_source[src]
+        else:
+            x = x if batch > 1 else x[0]
+            x_by_source[src] = x
         A = nm.nm_pack(W, mask, N, M)
         mats = [A] + [nm.PackedMatrix(A.values.clone(), A.masks.clone(), A.rows, A.K, N, M)
                       for _ in range(copies - 1)]
@@ -205,8 +217,7 @@ def build_workload(wl, N, M, batch, copies, device="cuda", keep_dense=False):
         del W, mask
         y = torch.empty(batch, layer.rows, dtype=torch.float16, device=device)
         layers.append(dict(name=layer.name, rows=layer.rows, K=layer.K, mats=mats,
-                           x=x if batch > 1 else x[0], y=y if batch > 1 else y[0], dense=dense,
-                           index=li))
+                           x=x, y=y if batch > 1 else y[0], dense=dense, index=li))
     torch.cuda.synchronize()
     return layers
 
@@ -216,15 +227,35 @@ def step_bytes(layers, batch):
     return [algorithmic_bytes(L["mats"][0], batch, 2) for L in layers]
 
 
-def capture_step_graphs(layers, copies):
+def capture_step_graphs(layers, copies, fused):
     from sparse_spmv_memory_02_b300.stream import LayerStream
     streams = []
     for c in range(copies):
         s = LayerStream([L["mats"][c] for L in layers], [L["x"] for L in layers],
-                        [L["y"] for L in layers])
+                        [L["y"] for L in layers], fuse_shared_input=fused)
         s.capture()
         streams.append(s)
     return streams
+
+
+def time_steps(streams, copies, steps, warmup, world):
+    """Replays `steps` steps (rotating over the copies) between CUDA events
+    after `warmup` untimed ones; returns (seconds, wall t0, wall t1)."""
+    for s in range(warmup):
+        streams[s % copies].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record()
+    for s in range(steps):
+        streams[s % copies].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    return e0.elapsed_time(e1) * 1e-3, t_wall0, t_wall1
 
 
 def layer_pass(layers, batch, reps, l2_bytes):
@@ -311,16 +342,22 @@ def dense_pass(layers, copies, steps, warmup):
 
 def e2e_pass(layers, streams, copies, steps, warmup, batch):
     """Through the public API with host buffers: per step, pinned-host x ->
-    device, the step's SpMV calls, device y -> pinned host, then the host
-    waits for y (a decode loop needs the result before the next token)."""
-    xs_h = [L["x"].detach().cpu().pin_memory() for L in layers]
+    device (each distinct input vector once), the step's SpMV launches,
+    device y -> pinned host, then the host waits for y (a decode loop needs
+    the result before the next token)."""
+    xs_dev, seen = [], set()
+    for L in layers:
+        if id(L["x"]) not in seen:
+            seen.add(id(L["x"]))
+            xs_dev.append(L["x"])
+    xs_h = [x.detach().cpu().pin_memory() for x in xs_dev]
     ys_h = [torch.empty(L["y"].shape, dtype=L["y"].dtype).pin_memory() for L in layers]
     h2d = sum(t.numel() * t.element_size() for t in xs_h)
     d2h = sum(t.numel() * t.element_size() for t in ys_h)
 
     def one(s):
-        for L, xh in zip(layers, xs_h):
-            L["x"].copy_(xh, non_blocking=True)
+        for xd, xh in zip(xs_dev, xs_h):
+            xd.copy_(xh, non_blocking=True)
         streams[s % copies].replay()
         for L, yh in zip(layers, ys_h):
             yh.copy_(L["y"], non_blocking=True)
@@ -405,10 +442,13 @@ def config_block(args, wl, N, M, copies, layers_desc):
     return {"workload": wl.key, "title": wl.title, "pattern": "%d:%d" % (N, M),
             "batch": args.batch, "layers": layers_desc,
             "l2": "rotating %d packed copies of the step's weights (> 3x the 126 MB L2)" % copies,
-            "launch": "one CUDA graph of %d nm_spmv calls per step" % len(layers_desc),
+            "launch": "one CUDA graph per step: %s" % (
+                "q/k/v and gate/up each one nm_spmv_group launch (they read the same input), "
+                "o and down one nm_spmv launch each" if getattr(args, "launch", "") == "fused"
+                else "one nm_spmv launch per layer"),
             "weights": "synthetic N(0,0.02), top-N |w| per group of M along K",
-            "activations": "synthetic N(0,1), 1% outlier channels x20" if wl.outliers
-            else "synthetic N(0,1)"}
+            "activations": ("synthetic N(0,1), 1% outlier channels x20; q/k/v share one input "
+                            "vector, gate/up another" if wl.outliers else "synthetic N(0,1)")}
 
 
 def run_reference(args, world, rank):
@@ -452,30 +492,22 @@ def run_ours(args, world, rank, local):
     layers = build_workload(wl, N, M, args.batch, copies, keep_dense=not args.no_dense)
     bytes_per_call = step_bytes(layers, args.batch)
     step_b = sum(bytes_per_call)
-    streams = capture_step_graphs(layers, copies)
+    variants = {"fused": capture_step_graphs(layers, copies, fused=True),
+                "unfused": capture_step_graphs(layers, copies, fused=False)}
+    streams = variants[args.launch]
+    other = "unfused" if args.launch == "fused" else "fused"
 
     sampler = ClockSampler(local).start() if rank == 0 else None
-    for s in range(args.warmup):
-        streams[s % copies].replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    e0.record()
-    for s in range(args.steps):
-        streams[s % copies].replay()
-    e1.record()
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier(world)
-    dt = e0.elapsed_time(e1) * 1e-3
+    dt, t_wall0, t_wall1 = time_steps(streams, copies, args.steps, args.warmup, world)
     dt = max_over_ranks(dt, world)
-    launches = len(layers) * args.steps
-
+    launches = streams[0].launches * args.steps
     if sampler is not None:
         sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    # the other launch structure of the same step, same protocol
+    odt, _, _ = time_steps(variants[other], copies, args.steps, args.warmup, world)
+    odt = max_over_ranks(odt, world)
+
     # each layer alone, L2-cold, for the per-layer figures
     l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     layer_t = layer_pass(layers, args.batch, args.profile_steps, l2_bytes)
@@ -497,8 +529,8 @@ def run_ours(args, world, rank, local):
                                 args.warmup, args.batch)
         e2e = {"value": step_b / et / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "us_per_step": et * 1e6,
-               "path": "pinned host x -> device, graph of nm_spmv calls, y -> pinned host, "
-                       "host waits each step"}
+               "path": "pinned host x -> device, the step's graph (%s), y -> pinned host, "
+                       "host waits each step" % args.launch}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -533,11 +565,16 @@ def run_ours(args, world, rank, local):
         "step_algorithmic_bytes": step_b,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,
+        "launch": {"structure": args.launch, "launches_per_step": streams[0].launches,
+                   "groups": [[layers[i]["name"] for i in g] for g in streams[0].groups],
+                   other: {"launches_per_step": variants[other][0].launches,
+                           "us_per_step": odt / args.steps * 1e6,
+                           "value": step_b * args.steps / odt / 1e9}},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": TRAFFIC_PER_LAUNCH.get(
-                         (wl.key, "%d:%d" % (N, M), args.batch)),
+                         (wl.key, "%d:%d" % (N, M), args.batch, args.launch)),
                      "kernel": "nm_spmv_rows_kernel (every one of the %d launches of a step)"
-                               % len(layers),
+                               % streams[0].launches,
                      "note": "achieved = algorithmic bytes per launch / average launch time over "
                              "the timed steps (CUDA events on the replay stream; the step's "
                              "launches are all this kernel, so this equals the step's GB/s); "

@@ -50,8 +50,9 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 100 /* 1.0.0 */
+#define NM_VERSION 110 /* 1.1.0 */
 #define NM_MAX_BATCH 8
+#define NM_MAX_GROUP 8
 
 /* A CUDA stream handle; identical to cudaStream_t. */
 typedef struct CUstream_st *nm_stream_t;
@@ -178,6 +179,29 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
 nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
                           void *y, int64_t ldy, int batch, nm_dtype y_type,
                           nm_stream_t stream);
+
+/*
+ * Several independent products in one launch: y_i = A_i x_i for i < count
+ * (0 <= count <= NM_MAX_GROUP), for the decode-step layers that share an
+ * input -- the query, key and value projections of a block all read the
+ * attention input, the gate and up projections the MLP input -- so that one
+ * launch streams all their weights (fewer launch boundaries per token).
+ *   A     host array of `count` packed matrices with the same N, M and K;
+ *         rows may differ.
+ *   x     host array of `count` device pointers, x[i] fp16 [batch][ldx]
+ *         (the same vector may appear several times).
+ *   y     host array of `count` device pointers, y[i] y_type [batch][ldy[i]].
+ *   ldy   host array of `count` leading dimensions (NULL: ldy[i] = rows_i).
+ *   batch, ldx, y_type, stream: as nm_spmv_batched, shared by all products.
+ * Each product's arguments are checked as by nm_spmv_batched (errors name
+ * the matrix); matrices that differ in N, M or K are NM_ERR_INVALID_ARG.
+ * When the shapes cannot share a launch the products are launched one by
+ * one, with the same results.  Asynchronous, allocates nothing, may be
+ * captured in a CUDA graph; the products' y must not overlap.
+ */
+nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
+                        void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
+                        nm_stream_t stream);
 
 /*
  * Read the device error word of the calling thread's current device into

@@ -5,6 +5,10 @@ keep-mask and fp16 activation vectors.  It holds none of the packing or
 product arithmetic, so both the CUDA path and the CPU oracle can take their
 inputs from it without sharing any of the method's code.
 
+Within a decoder block the query, key and value projections share one
+input vector (the attention input) and gate and up share another (the MLP
+input), as in the models' forward pass.
+
 Shapes are the decoder linear layers of the models named by the pages
 ("SparseDecoding Makes LLM Pruning Aware of Generation", Introduction:
 Llama-3.1-8B, Llama-3.3-70B, Qwen3-14B, Qwen3-32B).  No trained weights are
@@ -82,8 +86,27 @@ def weight_seed(workload: Workload, layer_index: int) -> int:
     return 1000 * workload.config_index + layer_index if workload.config_index != 1 else 0
 
 
+# Layers of a decoder block that read the same input vector: the query, key
+# and value projections read the attention input, gate and up the MLP input.
+SHARED_INPUT = {"k": "q", "v": "q", "up": "gate"}
+
+
+def x_source(workload: Workload, layer_index: int) -> int:
+    """Index of the layer whose input vector this layer reads (itself unless
+    it shares the block's attention or MLP input with an earlier layer)."""
+    n = len(workload.layers)
+    block, j = divmod(layer_index, n)
+    src = SHARED_INPUT.get(workload.layers[j].name)
+    if src is None:
+        return layer_index
+    for jj, layer in enumerate(workload.layers):
+        if layer.name == src:
+            return block * n + jj
+    return layer_index
+
+
 def x_seed(workload: Workload, layer_index: int) -> int:
-    return weight_seed(workload, layer_index) + 500
+    return weight_seed(workload, x_source(workload, layer_index)) + 500
 
 
 def _gen(seed: int, device) -> torch.Generator:

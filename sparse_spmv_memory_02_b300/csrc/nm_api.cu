@@ -25,13 +25,13 @@ cudaError_t launch_bulk_1_8(const SpmvProblem &, cudaStream_t);
 cudaError_t launch_bulk_2_8(const SpmvProblem &, cudaStream_t);
 cudaError_t launch_bulk_4_8(const SpmvProblem &, cudaStream_t);
 cudaError_t launch_bulk_8_8(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_1_4(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_2_4(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_4_4(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_1_8(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_2_8(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_4_8(const SpmvProblem &, cudaStream_t);
-cudaError_t launch_rows_8_8(const SpmvProblem &, cudaStream_t);
+cudaError_t launch_rows_1_4(const SpmvGroup &, cudaStream_t);
+cudaError_t launch_rows_2_4(const SpmvGroup &, cudaStream_t);
+cudaError_t launch_rows_4_4(const SpmvGroup &, cudaStream_t);
+cudaError_t launch_rows_1_8(const SpmvGroup &, cudaStream_t);
+cudaError_t launch_rows_2_8(const SpmvGroup &, cudaStream_t);
+cudaError_t launch_rows_4_8(const SpmvGroup &, cudaStream_t);
+cudaError_t launch_rows_8_8(const SpmvGroup &, cudaStream_t);
 
 bool fast_path_applies(int N, int M, int64_t K)
 {
@@ -46,16 +46,16 @@ bool bulk_path_applies(int N, int M, int64_t K)
     return fast_path_applies(N, M, K) && K % 128 == 0;
 }
 
-cudaError_t launch_rows(const SpmvProblem &p, cudaStream_t s)
+cudaError_t launch_rows(const SpmvGroup &g, cudaStream_t s)
 {
-    switch (p.M * 16 + p.N) {
-    case 4 * 16 + 1: return launch_rows_1_4(p, s);
-    case 4 * 16 + 2: return launch_rows_2_4(p, s);
-    case 4 * 16 + 4: return launch_rows_4_4(p, s);
-    case 8 * 16 + 1: return launch_rows_1_8(p, s);
-    case 8 * 16 + 2: return launch_rows_2_8(p, s);
-    case 8 * 16 + 4: return launch_rows_4_8(p, s);
-    case 8 * 16 + 8: return launch_rows_8_8(p, s);
+    switch (g.p[0].M * 16 + g.p[0].N) {
+    case 4 * 16 + 1: return launch_rows_1_4(g, s);
+    case 4 * 16 + 2: return launch_rows_2_4(g, s);
+    case 4 * 16 + 4: return launch_rows_4_4(g, s);
+    case 8 * 16 + 1: return launch_rows_1_8(g, s);
+    case 8 * 16 + 2: return launch_rows_2_8(g, s);
+    case 8 * 16 + 4: return launch_rows_4_8(g, s);
+    case 8 * 16 + 8: return launch_rows_8_8(g, s);
     default: return cudaErrorNotSupported;
     }
 }
@@ -167,6 +167,84 @@ nm_status check_matrix(const nm_matrix *A)
     return NM_OK;
 }
 
+// Checks the arguments of one product y = A x (batch vectors) and fills `p`.
+// Sets *empty, having done the whole job, when rows == 0 (nothing to do) or
+// K == 0 (y is zeroed on `s`).
+nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *y, int64_t ldy,
+                          int batch, nm_dtype y_type, nm::SpmvProblem *p, bool *empty,
+                          cudaStream_t s)
+{
+    *empty = false;
+    nm_status st = check_matrix(A);
+    if (st != NM_OK) return st;
+    if (batch < 1 || batch > NM_MAX_BATCH)
+        return fail(NM_ERR_INVALID_ARG, "batch=%d outside [1, %d]", batch, NM_MAX_BATCH);
+    if (y_type != NM_F16 && y_type != NM_F32)
+        return fail(NM_ERR_INVALID_ARG, "unknown y_type %d", (int)y_type);
+    const size_t esize = y_type == NM_F32 ? 4 : 2;
+    if (ldy < A->rows)
+        return fail(NM_ERR_INVALID_ARG, "ldy=%lld < rows=%lld", (long long)ldy, (long long)A->rows);
+    if (A->K > 0) {
+        if (ldx < A->K)
+            return fail(NM_ERR_INVALID_ARG, "ldx=%lld < K=%lld", (long long)ldx, (long long)A->K);
+        if (batch > 1 && ldx % 8 != 0)
+            return fail(NM_ERR_INVALID_ARG, "ldx=%lld must be a multiple of 8 when batch > 1",
+                        (long long)ldx);
+    }
+    if (A->rows == 0) {
+        *empty = true;
+        return NM_OK;
+    }
+    if (!y) return fail(NM_ERR_INVALID_ARG, "y is NULL");
+    if (!aligned(y, esize)) return fail(NM_ERR_INVALID_ARG, "y is not %zu-byte aligned", esize);
+    if (ldy > (INT64_MAX / 16) / batch) return fail(NM_ERR_INVALID_ARG, "ldy too large");
+    if (A->K == 0) {  // empty sums: y = 0
+        cudaError_t e = cudaMemset2DAsync(y, static_cast<size_t>(ldy) * esize, 0,
+                                          static_cast<size_t>(A->rows) * esize, batch, s);
+        if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: cudaMemset2DAsync");
+        *empty = true;
+        return NM_OK;
+    }
+    if (!x) return fail(NM_ERR_INVALID_ARG, "x is NULL");
+    if (!aligned(x, 16)) return fail(NM_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    if (ldx > (INT64_MAX / 16) / batch) return fail(NM_ERR_INVALID_ARG, "ldx too large");
+
+    p->rows = A->rows;
+    p->K = A->K;
+    p->N = A->N;
+    p->M = A->M;
+    p->values = A->values;
+    p->masks = A->masks;
+    p->x = x;
+    p->ldx = ldx;
+    p->y = y;
+    p->ldy = ldy;
+    p->batch = batch;
+    p->y_f32 = y_type == NM_F32;
+    cudaError_t e = device_error_word(&p->err);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: device error word");
+    return NM_OK;
+}
+
+// One product on the best kernel that applies: the row-per-warp kernel
+// (batch <= 2), the chunk-column kernel, the direct-load kernel, the scalar
+// kernel.
+nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)
+{
+    cudaError_t e = cudaErrorNotSupported;
+    if (nm::bulk_path_applies(p.N, p.M, p.K)) {
+        nm::SpmvGroup g;
+        g.count = 1;
+        g.p[0] = p;
+        e = nm::launch_rows(g, s);
+        if (e == cudaErrorNotSupported) e = nm::launch_bulk(p, s);
+    }
+    if (e == cudaErrorNotSupported)
+        e = nm::fast_path_applies(p.N, p.M, p.K) ? nm::launch_fast(p, s) : nm::launch_generic(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv launch");
+    return NM_OK;
+}
+
 }  // namespace
 
 void nm::set_last_error(const char *msg)
@@ -263,60 +341,56 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx, void *
                           int batch, nm_dtype y_type, nm_stream_t stream)
 {
     g_last_error[0] = 0;
-    nm_status st = check_matrix(A);
-    if (st != NM_OK) return st;
-    if (batch < 1 || batch > NM_MAX_BATCH)
-        return fail(NM_ERR_INVALID_ARG, "batch=%d outside [1, %d]", batch, NM_MAX_BATCH);
-    if (y_type != NM_F16 && y_type != NM_F32)
-        return fail(NM_ERR_INVALID_ARG, "unknown y_type %d", (int)y_type);
-    const size_t esize = y_type == NM_F32 ? 4 : 2;
-    if (ldy < A->rows)
-        return fail(NM_ERR_INVALID_ARG, "ldy=%lld < rows=%lld", (long long)ldy, (long long)A->rows);
-    if (A->K > 0) {
-        if (ldx < A->K)
-            return fail(NM_ERR_INVALID_ARG, "ldx=%lld < K=%lld", (long long)ldx, (long long)A->K);
-        if (batch > 1 && ldx % 8 != 0)
-            return fail(NM_ERR_INVALID_ARG, "ldx=%lld must be a multiple of 8 when batch > 1",
-                        (long long)ldx);
-    }
-    if (A->rows == 0) return NM_OK;
-    if (!y) return fail(NM_ERR_INVALID_ARG, "y is NULL");
-    if (!aligned(y, esize)) return fail(NM_ERR_INVALID_ARG, "y is not %zu-byte aligned", esize);
-    if (ldy > (INT64_MAX / 16) / batch) return fail(NM_ERR_INVALID_ARG, "ldy too large");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (A->K == 0) {  // empty sums: y = 0
-        cudaError_t e = cudaMemset2DAsync(y, static_cast<size_t>(ldy) * esize, 0,
-                                          static_cast<size_t>(A->rows) * esize, batch, s);
-        if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: cudaMemset2DAsync");
-        return NM_OK;
-    }
-    if (!x) return fail(NM_ERR_INVALID_ARG, "x is NULL");
-    if (!aligned(x, 16)) return fail(NM_ERR_INVALID_ARG, "x must be 16-byte aligned");
-    if (ldx > (INT64_MAX / 16) / batch) return fail(NM_ERR_INVALID_ARG, "ldx too large");
-
     nm::SpmvProblem p;
-    p.rows = A->rows;
-    p.K = A->K;
-    p.N = A->N;
-    p.M = A->M;
-    p.values = A->values;
-    p.masks = A->masks;
-    p.x = x;
-    p.ldx = ldx;
-    p.y = y;
-    p.ldy = ldy;
-    p.batch = batch;
-    p.y_f32 = y_type == NM_F32;
-    cudaError_t e = device_error_word(&p.err);
-    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: device error word");
-    e = cudaErrorNotSupported;
-    if (nm::bulk_path_applies(p.N, p.M, p.K)) {
-        e = nm::launch_rows(p, s);
-        if (e == cudaErrorNotSupported) e = nm::launch_bulk(p, s);
+    bool empty = false;
+    nm_status st = prepare_product(A, x, ldx, y, ldy, batch, y_type, &p, &empty,
+                                   reinterpret_cast<cudaStream_t>(stream));
+    if (st != NM_OK || empty) return st;
+    return run_product(p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
+                        void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
+                        nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    if (count < 0 || count > NM_MAX_GROUP)
+        return fail(NM_ERR_INVALID_ARG, "count=%d outside [0, %d]", count, NM_MAX_GROUP);
+    if (count == 0) return NM_OK;
+    if (!A || !x || !y) return fail(NM_ERR_INVALID_ARG, "A, x and y must be non-NULL arrays");
+    for (int i = 1; i < count; ++i)
+        if (A[i].N != A[0].N || A[i].M != A[0].M || A[i].K != A[0].K)
+            return fail(NM_ERR_INVALID_ARG, "matrix %d: N, M and K must equal those of matrix 0", i);
+    nm::SpmvGroup g;
+    g.count = 0;
+    bool fusable = true;
+    for (int i = 0; i < count; ++i) {
+        bool empty = false;
+        nm_status st = prepare_product(&A[i], x[i], ldx, y[i], ldy ? ldy[i] : A[i].rows, batch,
+                                       y_type, &g.p[g.count], &empty,
+                                       reinterpret_cast<cudaStream_t>(stream));
+        if (st != NM_OK) {
+            char msg[512];
+            snprintf(msg, sizeof(msg), "matrix %d: %s", i, g_last_error);
+            return fail(st, "%s", msg);
+        }
+        if (empty) {  // rows == 0 (nothing) or K == 0 (y zeroed already)
+            fusable = false;
+            continue;
+        }
+        ++g.count;
     }
-    if (e == cudaErrorNotSupported)
-        e = nm::fast_path_applies(p.N, p.M, p.K) ? nm::launch_fast(p, s) : nm::launch_generic(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv launch");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorNotSupported;
+    if (fusable && g.count > 1 && g.p[0].batch <= 2 &&
+        nm::bulk_path_applies(g.p[0].N, g.p[0].M, g.p[0].K))
+        e = nm::launch_rows(g, s);
+    if (e == cudaSuccess) return NM_OK;
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "nm_spmv_group launch");
+    for (int i = 0; i < g.count; ++i) {  // one launch per matrix
+        nm_status st = run_product(g.p[i], s);
+        if (st != NM_OK) return st;
+    }
     return NM_OK;
 }
 

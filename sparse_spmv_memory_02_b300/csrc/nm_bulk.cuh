@@ -130,13 +130,23 @@ nm_spmv_bulk_kernel(const BulkArgs a)
             const uint32_t mb = static_cast<uint32_t>(nc) * MB;
             mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(nr) * (vb + mb));
             uint8_t *st = ring + static_cast<size_t>(slot) * a.stage_bytes;
-            for (int i = 0; i < nr; ++i) {
-                const int64_t row = r_begin + i0 + i;
-                bulk_g2s(st + i * a.seg_v, a.values + row * a.vrow_bytes + c0 * 16LL, vb,
+            if (a.ktiles == 1) {
+                // whole rows (seg_v == vrow_bytes, seg_m == mrow_bytes): the
+                // stage's rows are one contiguous range of each array
+                const int64_t row0 = r_begin + i0;
+                bulk_g2s(st, a.values + row0 * a.vrow_bytes, static_cast<uint32_t>(nr) * vb,
                          &full[slot], pol);
-                bulk_g2s(st + a.R * a.seg_v + i * a.seg_m,
-                         a.masks + row * a.mrow_bytes + static_cast<int64_t>(c0) * MB, mb,
-                         &full[slot], pol);
+                bulk_g2s(st + a.R * a.seg_v, a.masks + row0 * a.mrow_bytes,
+                         static_cast<uint32_t>(nr) * mb, &full[slot], pol);
+            } else {
+                for (int i = 0; i < nr; ++i) {
+                    const int64_t row = r_begin + i0 + i;
+                    bulk_g2s(st + i * a.seg_v, a.values + row * a.vrow_bytes + c0 * 16LL, vb,
+                             &full[slot], pol);
+                    bulk_g2s(st + a.R * a.seg_v + i * a.seg_m,
+                             a.masks + row * a.mrow_bytes + static_cast<int64_t>(c0) * MB, mb,
+                             &full[slot], pol);
+                }
             }
         }
         // Do not leave while copies into this CTA's shared memory may still

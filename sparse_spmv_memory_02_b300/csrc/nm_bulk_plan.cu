@@ -107,8 +107,11 @@ bool bulk_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, B
     p.cpl = bc;
     p.tile_chunks = 32 * bw * bc;
     p.ktiles = (chunks + p.tile_chunks - 1) / p.tile_chunks;
-    p.seg_v = p.tile_chunks * 16;
-    p.seg_m = round_up(p.tile_chunks * MB, 16);
+    // With one K tile a stage's rows are copied as one contiguous range, so
+    // the shared row stride must be exactly the packed row.
+    const int seg_chunks = p.ktiles == 1 ? chunks : p.tile_chunks;
+    p.seg_v = seg_chunks * 16;
+    p.seg_m = round_up(seg_chunks * MB, 16);
     const int seg = p.seg_v + p.seg_m;
 
     // 2. Rows per stage and ring depth.
@@ -145,11 +148,14 @@ bool bulk_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, B
     return true;
 }
 
-bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, RowsPlan *out)
+namespace {
+
+// The row kernel's plan for a K (in chunks), batch and a grid whose busiest
+// CTA has rows_per_cta rows.
+bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, int max_smem,
+                    RowsPlan *out)
 {
-    if (rows <= 0 || chunks <= 0 || B < 1 || B > 2) return false;
     const BulkTuning &t = bulk_tuning();
-    if (!t.rows_kernel) return false;
     const int MB = CK / 8;  // mask bytes per chunk
     const int W = t.rows_warps ? t.rows_warps : 16;
     const int64_t row_bytes = static_cast<int64_t>(chunks) * (16 + MB);
@@ -161,6 +167,7 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, R
     for (int target = t.rows_task_bytes; target >= 1024; target /= 2) {
         RowsPlan p;
         p.W = W;
+        p.grid = grid;
         // 1. K tile: whole rows if a row fits the task and the x tile 48 KB;
         //    tiles are multiples of 32 chunks and split the row evenly.
         const int64_t seg_cap = std::min<int64_t>(target, t.rows_max_seg);
@@ -186,19 +193,10 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, R
         p.R = R;
         p.stage_bytes = R * seg;
 
-        // 3. Grid: one wave; more CTAs only if the carried partial sums of a
-        //    CTA's rows would not fit in 32 KB.
-        int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(nsm) * t.ctas_per_sm);
-        if (p.ktiles > 1) {
-            const int64_t max_rows = (32 * 1024) / (4 * B);
-            grid = std::max<int64_t>(grid, (rows + max_rows - 1) / max_rows);
-        }
-        if (grid > 0x7fffffff) return false;
-        p.grid = static_cast<int>(grid);
-        const int64_t rows_per_cta = (rows + grid - 1) / grid;
-        const int carry = p.ktiles > 1 ? static_cast<int>(rows_per_cta * B * 4) : 0;
-
-        // 4. Shared memory: slots [W][SW] | x buffers | barriers | carry.
+        // 3. Shared memory: slots [W][SW] | x buffers | barriers | carry.
+        const int64_t carry64 = p.ktiles > 1 ? rows_per_cta * B * 4 : 0;
+        if (carry64 > 64 * 1024) return false;
+        const int carry = static_cast<int>(carry64);
         p.xbuf_bytes = B * (CK / 8) * p.tile_chunks * 16;
         const int nxb = p.ktiles > 1 ? 2 : 1;
         int SW = std::max(2, std::min(4, t.rows_ring_bytes / (W * p.stage_bytes)));
@@ -219,6 +217,73 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, R
         return true;
     }
     return false;
+}
+
+}  // namespace
+
+bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, RowsPlan *out)
+{
+    if (rows <= 0 || chunks <= 0 || B < 1 || B > 2) return false;
+    const BulkTuning &t = bulk_tuning();
+    if (!t.rows_kernel) return false;
+    // One wave of CTAs; more only if the carried partial sums of a CTA's rows
+    // would not fit (they are bounded by 32 KB here).
+    int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(nsm) * t.ctas_per_sm);
+    const int64_t max_rows = (32 * 1024) / (4 * B);
+    grid = std::max<int64_t>(grid, (rows + max_rows - 1) / max_rows);
+    if (grid > 0x7fffffff) return false;
+    return rows_plan_impl((rows + grid - 1) / grid, static_cast<int>(grid), chunks, CK, B,
+                          max_smem, out);
+}
+
+bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
+                     int max_smem, RowsPlan *out, int *cta_begin)
+{
+    if (count < 1 || count > kRowsMaxGroup || chunks <= 0 || B < 1 || B > 2) return false;
+    const BulkTuning &t = bulk_tuning();
+    if (!t.rows_kernel) return false;
+    int64_t total = 0;
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] <= 0) return false;
+        total += rows[i];
+    }
+    const int G = static_cast<int>(std::min<int64_t>(total, static_cast<int64_t>(nsm) * t.ctas_per_sm));
+    if (G < count) return false;
+    // CTAs in proportion to rows (largest remainder), at least one and at
+    // most rows[i] each.
+    int g[kRowsMaxGroup];
+    double frac[kRowsMaxGroup];
+    int used = 0;
+    for (int i = 0; i < count; ++i) {
+        const double share = static_cast<double>(G) * rows[i] / total;
+        g[i] = static_cast<int>(std::min<int64_t>(rows[i], std::max<int64_t>(1, static_cast<int64_t>(share))));
+        frac[i] = share - g[i];
+        used += g[i];
+    }
+    while (used < G) {  // hand out the rest by largest remainder
+        int best = -1;
+        for (int i = 0; i < count; ++i)
+            if (g[i] < rows[i] && (best < 0 || frac[i] > frac[best])) best = i;
+        if (best < 0) break;
+        ++g[best];
+        frac[best] -= 1.0;
+        ++used;
+    }
+    while (used > G) {  // the at-least-one rule overshot: take from the largest
+        int best = 0;
+        for (int i = 1; i < count; ++i)
+            if (g[i] > g[best]) best = i;
+        if (g[best] <= 1) return false;
+        --g[best];
+        --used;
+    }
+    int64_t rpc = 0;
+    cta_begin[0] = 0;
+    for (int i = 0; i < count; ++i) {
+        rpc = std::max<int64_t>(rpc, (rows[i] + g[i] - 1) / g[i]);
+        cta_begin[i + 1] = cta_begin[i] + g[i];
+    }
+    return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, out);
 }
 
 }  // namespace nm

@@ -13,8 +13,8 @@ cudaError_t launch_bulk_2_8(const SpmvProblem &p, cudaStream_t s)
 {
     return launch_bulk_pattern<2, 8>(p, s);
 }
-cudaError_t launch_rows_2_8(const SpmvProblem &p, cudaStream_t s)
+cudaError_t launch_rows_2_8(const SpmvGroup &g, cudaStream_t s)
 {
-    return launch_rows_pattern<2, 8>(p, s);
+    return launch_rows_pattern<2, 8>(g, s);
 }
 }  // namespace nm

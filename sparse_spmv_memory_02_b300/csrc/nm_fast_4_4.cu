@@ -13,8 +13,8 @@ cudaError_t launch_bulk_4_4(const SpmvProblem &p, cudaStream_t s)
 {
     return launch_bulk_pattern<4, 4>(p, s);
 }
-cudaError_t launch_rows_4_4(const SpmvProblem &p, cudaStream_t s)
+cudaError_t launch_rows_4_4(const SpmvGroup &g, cudaStream_t s)
 {
-    return launch_rows_pattern<4, 4>(p, s);
+    return launch_rows_pattern<4, 4>(g, s);
 }
 }  // namespace nm

@@ -26,6 +26,13 @@ struct SpmvProblem {
     unsigned int *err;  // device error word (see nm_device_errors)
 };
 
+// Independent products fused into one launch: same N, M, K, batch, ldx and
+// y type; rows, pointers and ldy per problem.
+struct SpmvGroup {
+    int count;
+    SpmvProblem p[NM_MAX_GROUP];
+};
+
 // Vectorised kernel: 8 % N == 0 and K a multiple of the k-span of one
 // 16-byte value chunk (8*M/N positions), and at most kMaxFastChunks chunks
 // per K tile sweep (any K is handled by tiling K inside a block).
@@ -38,7 +45,7 @@ cudaError_t launch_fast(const SpmvProblem &p, cudaStream_t s);
 // (chunk columns per thread, any batch).  Both return cudaErrorNotSupported,
 // having launched nothing, if no tiling fits in shared memory.
 bool bulk_path_applies(int N, int M, int64_t K);
-cudaError_t launch_rows(const SpmvProblem &p, cudaStream_t s);  // batch <= 2
+cudaError_t launch_rows(const SpmvGroup &g, cudaStream_t s);  // batch <= 2
 cudaError_t launch_bulk(const SpmvProblem &p, cudaStream_t s);
 
 // Scalar kernel for every valid pattern and K (patterns like 3:4, or K not

@@ -50,14 +50,26 @@
 
 namespace nm {
 
-struct RowsArgs {
+// One matrix of a launch (a launch may fuse up to kRowsMaxGroup independent
+// products with the same pattern, batch and K; each CTA works on exactly one
+// of them).
+constexpr int kRowsMaxGroup = NM_MAX_GROUP;
+struct RowsMat {
     const uint8_t *values;  // [rows][vrow_bytes]
     const uint8_t *masks;   // [rows][mrow_bytes]
     const __half *x;        // [B][ldx]
     void *y;                // [B][ldy]
+    int64_t ldy;
+    int cta_begin;          // first CTA of this matrix
+    int row_base, row_extra;  // its CTA c owns row_base rows (+1 if c < row_extra)
+};
+
+struct RowsArgs {
+    RowsMat mat[kRowsMaxGroup];
+    int nmat;
     unsigned int *err;      // device error word
-    int64_t ldx, ldy, vrow_bytes, mrow_bytes;
-    int rows, chunks;       // 16-byte value chunks per row
+    int64_t ldx, vrow_bytes, mrow_bytes;
+    int chunks;             // 16-byte value chunks per row
     int tile_chunks;        // chunks per K tile
     int ktiles;
     int SW;                 // slots per warp
@@ -65,7 +77,6 @@ struct RowsArgs {
     int stage_bytes;        // R * (seg_v + seg_m)
     int xbuf_bytes;         // one x tile buffer: B * XV * tile_chunks * 16
     int off_x, off_bar, off_carry;
-    int row_base, row_extra;  // CTA c owns row_base rows (+1 if c < row_extra)
     int y_f32;
     int pf_bytes;           // bytes of values (and matching masks) warmed in L2 per CTA
 };
@@ -83,8 +94,9 @@ __device__ __forceinline__ RowsTask rows_task(int j, int w, int W, int per_kt)
 }
 
 template <int R, int MB>
-__device__ __forceinline__ void rows_issue(const RowsArgs &a, uint8_t *st, uint64_t *bar, int kt,
-                                           int i0, int nr, int r_begin, uint64_t pol)
+__device__ __forceinline__ void rows_issue(const RowsArgs &a, const uint8_t *values,
+                                           const uint8_t *masks, uint8_t *st, uint64_t *bar,
+                                           int kt, int i0, int nr, int r_begin, uint64_t pol)
 {
     const int c0 = kt * a.tile_chunks;
     const int nc = min(a.tile_chunks, a.chunks - c0);
@@ -95,22 +107,22 @@ __device__ __forceinline__ void rows_issue(const RowsArgs &a, uint8_t *st, uint6
     if (a.ktiles == 1) {
         // whole rows: seg_v == vrow_bytes and seg_m == mrow_bytes, so the
         // rows are one contiguous range of each array, in the slot's layout
-        bulk_g2s(st, a.values + row0 * a.vrow_bytes, static_cast<uint32_t>(nr) * vb, bar, pol);
-        bulk_g2s(st + R * a.seg_v, a.masks + row0 * a.mrow_bytes, static_cast<uint32_t>(nr) * mb,
+        bulk_g2s(st, values + row0 * a.vrow_bytes, static_cast<uint32_t>(nr) * vb, bar, pol);
+        bulk_g2s(st + R * a.seg_v, masks + row0 * a.mrow_bytes, static_cast<uint32_t>(nr) * mb,
                  bar, pol);
     } else {
         for (int i = 0; i < nr; ++i) {
             const int64_t row = row0 + i;
-            bulk_g2s(st + i * a.seg_v, a.values + row * a.vrow_bytes + c0 * 16LL, vb, bar, pol);
+            bulk_g2s(st + i * a.seg_v, values + row * a.vrow_bytes + c0 * 16LL, vb, bar, pol);
             bulk_g2s(st + R * a.seg_v + i * a.seg_m,
-                     a.masks + row * a.mrow_bytes + static_cast<int64_t>(c0) * MB, mb, bar, pol);
+                     masks + row * a.mrow_bytes + static_cast<int64_t>(c0) * MB, mb, bar, pol);
         }
     }
 }
 
 template <int N, int M, int B, int R>
 __global__ void __launch_bounds__(32 * kRowsMaxWarps, 1)
-nm_spmv_rows_kernel(const RowsArgs a)
+nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 {
     using P = Pattern<N, M>;
     using mask_t = typename P::mask_t;
@@ -137,9 +149,13 @@ nm_spmv_rows_kernel(const RowsArgs a)
     __syncthreads();
     pdl_launch_dependents();
 
-    const int cta = blockIdx.x;
-    const int r_begin = cta * a.row_base + min(cta, a.row_extra);
-    const int r_count = a.row_base + (cta < a.row_extra ? 1 : 0);
+    // The matrix this CTA works on, and its rows of it.
+    int mi = 0;
+    while (mi + 1 < a.nmat && static_cast<int>(blockIdx.x) >= a.mat[mi + 1].cta_begin) ++mi;
+    const RowsMat &mt = a.mat[mi];
+    const int cta = static_cast<int>(blockIdx.x) - mt.cta_begin;
+    const int r_begin = cta * mt.row_base + min(cta, mt.row_extra);
+    const int r_count = mt.row_base + (cta < mt.row_extra ? 1 : 0);
     const int nrt = (r_count + R - 1) / R;                         // row tiles of the CTA
     const int per_kt = nrt > warp ? (nrt - warp + W - 1) / W : 0;  // this warp's tiles per K tile
     const int ntask = per_kt * a.ktiles;
@@ -157,8 +173,8 @@ nm_spmv_rows_kernel(const RowsArgs a)
         const int64_t mtot = static_cast<int64_t>(r_count) * a.mrow_bytes;
         const int64_t vlen = min(vtot, static_cast<int64_t>(a.pf_bytes));
         const int64_t mlen = min(mtot, vlen / (a.vrow_bytes / a.mrow_bytes)) / 16 * 16;
-        const uint8_t *vsrc = a.values + static_cast<int64_t>(r_begin) * a.vrow_bytes;
-        const uint8_t *msrc = a.masks + static_cast<int64_t>(r_begin) * a.mrow_bytes;
+        const uint8_t *vsrc = mt.values + static_cast<int64_t>(r_begin) * a.vrow_bytes;
+        const uint8_t *msrc = mt.masks + static_cast<int64_t>(r_begin) * a.mrow_bytes;
         constexpr int64_t kPiece = 32768;
         for (int64_t off = static_cast<int64_t>(lane) * kPiece; off < vlen; off += 32 * kPiece)
             prefetch_l2(vsrc + off, static_cast<uint32_t>(min(kPiece, vlen - off)));
@@ -172,7 +188,8 @@ nm_spmv_rows_kernel(const RowsArgs a)
     if (lane == 0) {
         for (; issued < a.SW && issued < ntask; ++issued) {
             const RowsTask t = rows_task(issued, warp, W, per_kt);
-            rows_issue<R, MB>(a, my_ring + static_cast<size_t>(issued) * a.stage_bytes,
+            rows_issue<R, MB>(a, mt.values, mt.masks,
+                              my_ring + static_cast<size_t>(issued) * a.stage_bytes,
                               &my_full[issued], t.kt, t.rt * R, min(R, r_count - t.rt * R),
                               r_begin, pol);
         }
@@ -195,7 +212,7 @@ nm_spmv_rows_kernel(const RowsArgs a)
             const int b = e / (XV * nc);
             const int r = e - b * (XV * nc);
             const int c = r / XV, u = r - (r / XV) * XV;
-            const uint4 t = ld_cg_v4(a.x + b * a.ldx + static_cast<int64_t>(c0 + c) * CK + 8 * u);
+            const uint4 t = ld_cg_v4(mt.x + b * a.ldx + static_cast<int64_t>(c0 + c) * CK + 8 * u);
             *reinterpret_cast<uint4 *>(xs + ((b * XV + u) * a.tile_chunks + c) * 16) = t;
         }
         named_barrier_sync(1, blockDim.x);
@@ -248,7 +265,7 @@ nm_spmv_rows_kernel(const RowsArgs a)
             if (lane == 0 && issued < ntask && !failed) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 const RowsTask t = rows_task(issued, warp, W, per_kt);
-                rows_issue<R, MB>(a, sv, &my_full[slot], t.kt, t.rt * R,
+                rows_issue<R, MB>(a, mt.values, mt.masks, sv, &my_full[slot], t.kt, t.rt * R,
                                   min(R, r_count - t.rt * R), r_begin, pol);
                 ++issued;
             }
@@ -264,7 +281,7 @@ nm_spmv_rows_kernel(const RowsArgs a)
                     *cp = tot;
                 }
                 if (kt == a.ktiles - 1)
-                    store_y(a.y, b * a.ldy + r_begin + i0 + i, tot, a.y_f32 != 0);
+                    store_y(mt.y, b * mt.ldy + r_begin + i0 + i, tot, a.y_f32 != 0);
             }
         }
     }
@@ -285,11 +302,15 @@ struct RowsPlan {
 
 // Chooses rows per task, K tile, warps and slots per warp for a shape;
 // false if nothing fits in shared memory (the caller then takes another
-// kernel).
+// kernel).  rows_plan_group does the same for `count` matrices with the same
+// K in one launch and writes each matrix's first CTA to cta_begin[0..count].
 bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, RowsPlan *out);
+bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
+                     int max_smem, RowsPlan *out, int *cta_begin);
 
 template <int N, int M, int B, int R>
-cudaError_t launch_rows_instance(const SpmvProblem &p, const RowsPlan &pl, cudaStream_t s)
+cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const int *cta_begin,
+                                 cudaStream_t s)
 {
     auto kernel = nm_spmv_rows_kernel<N, M, B, R>;
     static std::atomic<int> smem_set[64];
@@ -307,18 +328,27 @@ cudaError_t launch_rows_instance(const SpmvProblem &p, const RowsPlan &pl, cudaS
         }
     }
     using P = Pattern<N, M>;
-    RowsArgs a;
-    a.values = static_cast<const uint8_t *>(p.values);
-    a.masks = reinterpret_cast<const uint8_t *>(p.masks);
-    a.x = static_cast<const __half *>(p.x);
-    a.y = p.y;
-    a.err = p.err;
-    a.ldx = p.ldx;
-    a.ldy = p.ldy;
-    a.vrow_bytes = p.K / P::CK * 16;
-    a.mrow_bytes = ((p.K + 31) / 32) * 4;
-    a.rows = static_cast<int>(p.rows);
-    a.chunks = static_cast<int>(p.K / P::CK);
+    const SpmvProblem &p0 = g.p[0];
+    RowsArgs a = {};
+    for (int i = 0; i < g.count; ++i) {
+        const SpmvProblem &p = g.p[i];
+        RowsMat &m = a.mat[i];
+        m.values = static_cast<const uint8_t *>(p.values);
+        m.masks = reinterpret_cast<const uint8_t *>(p.masks);
+        m.x = static_cast<const __half *>(p.x);
+        m.y = p.y;
+        m.ldy = p.ldy;
+        m.cta_begin = cta_begin[i];
+        const int ctas = cta_begin[i + 1] - cta_begin[i];
+        m.row_base = static_cast<int>(p.rows / ctas);
+        m.row_extra = static_cast<int>(p.rows % ctas);
+    }
+    a.nmat = g.count;
+    a.err = p0.err;
+    a.ldx = p0.ldx;
+    a.vrow_bytes = p0.K / P::CK * 16;
+    a.mrow_bytes = ((p0.K + 31) / 32) * 4;
+    a.chunks = static_cast<int>(p0.K / P::CK);
     a.tile_chunks = pl.tile_chunks;
     a.ktiles = pl.ktiles;
     a.SW = pl.SW;
@@ -329,13 +359,11 @@ cudaError_t launch_rows_instance(const SpmvProblem &p, const RowsPlan &pl, cudaS
     a.off_x = pl.off_x;
     a.off_bar = pl.off_bar;
     a.off_carry = pl.off_carry;
-    a.row_base = a.rows / pl.grid;
-    a.row_extra = a.rows % pl.grid;
-    a.y_f32 = p.y_f32 ? 1 : 0;
+    a.y_f32 = p0.y_f32 ? 1 : 0;
     a.pf_bytes = bulk_tuning().l2_prefetch_bytes;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.grid);
+    cfg.gridDim = dim3(cta_begin[g.count]);
     cfg.blockDim = dim3(32 * pl.W);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
@@ -348,31 +376,47 @@ cudaError_t launch_rows_instance(const SpmvProblem &p, const RowsPlan &pl, cudaS
 }
 
 template <int N, int M, int B>
-cudaError_t launch_rows_b(const SpmvProblem &p, const RowsPlan &pl, cudaStream_t s)
+cudaError_t launch_rows_b(const SpmvGroup &g, const RowsPlan &pl, const int *cta_begin,
+                          cudaStream_t s)
 {
     switch (pl.R) {
-    case 1: return launch_rows_instance<N, M, B, 1>(p, pl, s);
-    case 2: return launch_rows_instance<N, M, B, 2>(p, pl, s);
-    case 4: return launch_rows_instance<N, M, B, 4>(p, pl, s);
+    case 1: return launch_rows_instance<N, M, B, 1>(g, pl, cta_begin, s);
+    case 2: return launch_rows_instance<N, M, B, 2>(g, pl, cta_begin, s);
+    case 4: return launch_rows_instance<N, M, B, 4>(g, pl, cta_begin, s);
     default: return cudaErrorNotSupported;
     }
 }
 
 // Batch 1 and 2 only; cudaErrorNotSupported (nothing launched) otherwise or
-// when no plan fits.
+// when no plan fits.  All problems of the group share N, M, K, batch, ldx
+// and the y type.
 template <int N, int M>
-cudaError_t launch_rows_pattern(const SpmvProblem &p, cudaStream_t s)
+cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
 {
     using P = Pattern<N, M>;
-    if (p.batch > 2) return cudaErrorNotSupported;
+    const SpmvProblem &p0 = g.p[0];
+    if (p0.batch > 2 || g.count < 1 || g.count > kRowsMaxGroup) return cudaErrorNotSupported;
     const int nsm = sm_count();
     if (nsm <= 0) return cudaErrorInvalidDevice;
     const int max_smem = max_dynamic_smem();
     if (max_smem <= 0) return cudaErrorInvalidDevice;
     RowsPlan pl;
-    if (!rows_plan(p.rows, static_cast<int>(p.K / P::CK), P::CK, p.batch, nsm, max_smem, &pl))
-        return cudaErrorNotSupported;
-    return p.batch == 1 ? launch_rows_b<N, M, 1>(p, pl, s) : launch_rows_b<N, M, 2>(p, pl, s);
+    int cta_begin[kRowsMaxGroup + 1];
+    const int chunks = static_cast<int>(p0.K / P::CK);
+    if (g.count == 1) {
+        if (!rows_plan(p0.rows, chunks, P::CK, p0.batch, nsm, max_smem, &pl))
+            return cudaErrorNotSupported;
+        cta_begin[0] = 0;
+        cta_begin[1] = pl.grid;
+    } else {
+        int64_t rows[kRowsMaxGroup];
+        for (int i = 0; i < g.count; ++i) rows[i] = g.p[i].rows;
+        if (!rows_plan_group(rows, g.count, chunks, P::CK, p0.batch, nsm, max_smem, &pl,
+                             cta_begin))
+            return cudaErrorNotSupported;
+    }
+    return p0.batch == 1 ? launch_rows_b<N, M, 1>(g, pl, cta_begin, s)
+                         : launch_rows_b<N, M, 2>(g, pl, cta_begin, s);
 }
 
 }  // namespace nm

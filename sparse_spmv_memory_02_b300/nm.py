@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libnm.so")
 NM_OK, NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_BAD_MASK, NM_ERR_CUDA = 0, 1, 2, 3, 4
 NM_F16, NM_F32 = 0, 1
 NM_MAX_BATCH = 8
+NM_MAX_GROUP = 8
 
 
 class NMError(RuntimeError):
@@ -71,6 +72,9 @@ def lib() -> ctypes.CDLL:
             L.nm_version.restype = ctypes.c_int
             L.nm_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32, vp]
             L.nm_device_errors.restype = ctypes.c_int
+            L.nm_spmv_group.argtypes = [mp, i32, ctypes.POINTER(vp), i64, ctypes.POINTER(vp),
+                                        ctypes.POINTER(i64), i32, i32, vp]
+            L.nm_spmv_group.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -209,3 +213,33 @@ def nm_spmv_batched(A: PackedMatrix, x: torch.Tensor, y: torch.Tensor | None = N
     _check(lib().nm_spmv_batched(ctypes.byref(A.desc), _ptr(x), ldx, _ptr(y), ldy, batch, yt,
                                  _stream(stream)))
     return y
+
+
+def nm_spmv_group(mats, xs, ys=None, y_dtype=torch.float16, stream=None):
+    """y_i = A_i x_i for several matrices with the same N, M and K in one
+    launch.  xs: one fp16 tensor per matrix, [K] or [batch][ldx] (the same
+    tensor may be passed several times, e.g. q/k/v sharing the attention
+    input); all share batch and ldx.  Returns the list of y tensors."""
+    mats, xs = list(mats), list(xs)
+    if len(mats) != len(xs):
+        raise ValueError("need one x per matrix")
+    count = len(mats)
+    if count == 0:
+        return []
+    for i, x in enumerate(xs):
+        _check_vec(x, "x[%d]" % i)
+    vec = xs[0].dim() == 1
+    batch = 1 if vec else xs[0].shape[0]
+    ldx = xs[0].shape[-1] if (vec or batch == 1) else xs[0].stride(0)
+    if ys is None:
+        ys = [torch.empty(A.rows, dtype=y_dtype, device=xs[0].device) if vec else
+              torch.empty(batch, A.rows, dtype=y_dtype, device=xs[0].device) for A in mats]
+    ys = list(ys)
+    yt = NM_F32 if ys[0].dtype == torch.float32 else NM_F16
+    descs = (nm_matrix * count)(*[A.desc for A in mats])
+    xp = (ctypes.c_void_p * count)(*[_ptr(x) for x in xs])
+    yp = (ctypes.c_void_p * count)(*[_ptr(y) for y in ys])
+    ldy = (ctypes.c_int64 * count)(*[(y.stride(0) if (y.dim() > 1 and batch > 1) else y.shape[-1])
+                                     for y in ys])
+    _check(lib().nm_spmv_group(descs, count, xp, ldx, yp, ldy, batch, yt, _stream(stream)))
+    return ys

@@ -5,31 +5,61 @@ linear layers of the model (decoding is dominated by SpMV: "SparseDecoding:
 Decoding-Aware Pruning for Accurate and Efficient LLM Inference", Abstract).
 ``LayerStream`` holds the packed matrices with their input and output
 buffers, records the whole sequence once into a CUDA graph and replays it per
-token, so one graph launch replaces hundreds of host-side launches.  Each
-call is an ``nm_spmv_batched`` launch of libnm; nothing else runs.
+token, so one graph launch replaces hundreds of host-side launches.  Layers
+that read the same input vector (the query, key and value projections; gate
+and up) can be fused into one ``nm_spmv_group`` launch.  Every launch is a
+libnm kernel; nothing else runs.
 """
 from __future__ import annotations
 
 import torch
 
-from .nm import PackedMatrix, nm_spmv, nm_spmv_batched
+from .nm import PackedMatrix, nm_spmv, nm_spmv_batched, nm_spmv_group
+
+
+def shared_input_groups(xs, mats):
+    """Consecutive layers reading the same x tensor with the same pattern and
+    K, as lists of indices (singletons for the others)."""
+    groups = []
+    for i, (x, A) in enumerate(zip(xs, mats)):
+        if groups:
+            j = groups[-1][0]
+            if (xs[j] is x and mats[j].K == A.K and mats[j].N == A.N and mats[j].M == A.M
+                    and len(groups[-1]) < 8):
+                groups[-1].append(i)
+                continue
+        groups.append([i])
+    return groups
 
 
 class LayerStream:
-    def __init__(self, mats, xs, ys):
+    def __init__(self, mats, xs, ys, fuse_shared_input: bool = False):
         """mats: PackedMatrix list; xs[i]: fp16 [batch][K_i] (or [K_i]);
-        ys[i]: fp16/fp32 [batch][rows_i] (or [rows_i]), preallocated."""
+        ys[i]: fp16/fp32 [batch][rows_i] (or [rows_i]), preallocated.  With
+        fuse_shared_input, consecutive layers passed the same x tensor are
+        computed by one grouped launch."""
         assert len(mats) == len(xs) == len(ys)
         self.mats = list(mats)
         self.xs = list(xs)
         self.ys = list(ys)
+        self.groups = (shared_input_groups(self.xs, self.mats) if fuse_shared_input
+                       else [[i] for i in range(len(self.mats))])
         self.graph = None
 
     def __len__(self):
         return len(self.mats)
 
+    @property
+    def launches(self) -> int:
+        return len(self.groups)
+
     def run_eager(self, stream=None):
-        for A, x, y in zip(self.mats, self.xs, self.ys):
+        for g in self.groups:
+            if len(g) > 1:
+                nm_spmv_group([self.mats[i] for i in g], [self.xs[i] for i in g],
+                              [self.ys[i] for i in g], stream=stream)
+                continue
+            A, x, y = self.mats[g[0]], self.xs[g[0]], self.ys[g[0]]
             if x.dim() == 1:
                 nm_spmv(A, x, y, stream=stream)
             else:

@@ -32,6 +32,30 @@ def test_header_declares_the_interface():
             "nm_version"} <= set(declared_functions())
 
 
+def test_spmv_group_checks_arguments_on_the_host():
+    L = nm.lib()
+    A = nm.nm_matrix(16, 64, 2, 4, A16, B16)
+    B = nm.nm_matrix(16, 128, 2, 4, A16, B16)
+    xp = (ctypes.c_void_p * 2)(C16, C16)
+    yp = (ctypes.c_void_p * 2)(D16, D16 + 4096)
+    mixed = (nm.nm_matrix * 2)(A, B)
+    assert L.nm_spmv_group(mixed, 2, xp, 128, yp, None, 1, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert "matrix 1" in nm.nm_last_error()
+    assert L.nm_spmv_group(mixed, nm.NM_MAX_GROUP + 1, xp, 128, yp, None, 1, nm.NM_F16,
+                           None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_group(mixed, -1, xp, 128, yp, None, 1, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_group(mixed, 0, xp, 128, yp, None, 1, nm.NM_F16, None) == nm.NM_OK
+    assert L.nm_spmv_group(None, 1, xp, 128, yp, None, 1, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    same = (nm.nm_matrix * 2)(A, A)
+    # per-matrix checks name the matrix: batch out of range
+    assert L.nm_spmv_group(same, 2, xp, 64, yp, None, 9, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert nm.nm_last_error().startswith("matrix 0")
+    # misaligned x of the second matrix
+    xbad = (ctypes.c_void_p * 2)(C16, C16 + 2)
+    st = L.nm_spmv_group(same, 2, xbad, 64, yp, None, 1, nm.NM_F16, None)
+    assert st in (nm.NM_ERR_INVALID_ARG, nm.NM_ERR_CUDA)
+
+
 def test_device_errors_rejects_null_on_the_host():
     assert nm.lib().nm_device_errors(None, 0, None) == nm.NM_ERR_INVALID_ARG
     assert "NULL" in nm.nm_last_error()

@@ -132,6 +132,77 @@ def test_dependent_chain_in_cuda_graph():
         assert torch.equal(y, ref)
 
 
+# ------------------------------------------------------------------ groups
+
+def _group_case(shapes, K, N, M, B, shared_x, seed):
+    mats, Ws, masks, xs = [], [], [], []
+    x0 = nm_synth.activations(K, B, seed + 500, True, DEV)
+    for i, rows in enumerate(shapes):
+        W = nm_synth.weights(rows, K, seed + i, DEV)
+        mask = nm_synth.topn_mask(W, N, M)
+        Ws.append(W)
+        masks.append(mask)
+        mats.append(nm.nm_pack(W, mask, N, M))
+        xs.append(x0 if shared_x else nm_synth.activations(K, B, seed + 600 + i, True, DEV))
+    return mats, Ws, masks, xs
+
+
+@pytest.mark.parametrize("shapes,K,N,M,B,shared", [
+    ((4096, 1024, 1024), 4096, 2, 4, 1, True),     # q/k/v of the 8B block
+    ((700, 300, 1), 4096, 2, 4, 1, False),
+    ((1500, 1500), 4096, 2, 4, 2, True),             # gate/up, batch 2
+    ((333, 77, 250, 4, 5, 6, 7, 900), 1024, 4, 8, 1, False),  # 8 matrices
+    ((512, 640), 14336, 2, 4, 1, True),              # rows span several K tiles
+    ((300, 200), 5120, 1, 4, 2, False),
+])
+def test_group_matches_oracle(shapes, K, N, M, B, shared):
+    mats, Ws, masks, xs = _group_case(shapes, K, N, M, B, shared, seed=sum(shapes) + K + B)
+    xin = [x[0] for x in xs] if B == 1 else xs
+    ys = [torch.full((A.rows,) if B == 1 else (B, A.rows), float("nan"),
+                     dtype=torch.float32, device=DEV) for A in mats]
+    nm.nm_spmv_group(mats, xin, ys)
+    torch.cuda.synchronize()
+    for y, W, mask, x in zip(ys, Ws, masks, xs):
+        _check(y if B > 1 else y[None], W, mask, x)
+    assert nm.nm_device_errors() == 0
+
+
+@pytest.mark.parametrize("K,B", [(4112, 1), (1024, 3), (4096, 8)])
+def test_group_falls_back_to_single_launches(K, B):
+    """Shapes the fused launch does not take (K not a multiple of 128, batch
+    above 2) still give every product."""
+    mats, Ws, masks, xs = _group_case((100, 37, 260), K, 2, 4, B, False, seed=K + B)
+    ys = nm.nm_spmv_group(mats, xs if B > 1 else [x[0] for x in xs], y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for y, W, mask, x in zip(ys, Ws, masks, xs):
+        _check(y if B > 1 else y[None], W, mask, x)
+
+
+def test_group_with_empty_member_and_graph_capture():
+    mats, Ws, masks, xs = _group_case((400, 300), 4096, 2, 4, 1, True, seed=5)
+    empty = nm.nm_pack(torch.empty(0, 4096, dtype=torch.float16, device=DEV),
+                       torch.empty(0, 4096, dtype=torch.uint8, device=DEV), 2, 4)
+    ye = torch.empty(0, dtype=torch.float32, device=DEV)
+    y0 = torch.empty(400, dtype=torch.float32, device=DEV)
+    y1 = torch.empty(300, dtype=torch.float32, device=DEV)
+    nm.nm_spmv_group([mats[0], empty, mats[1]], [xs[0][0]] * 3, [y0, ye, y1])
+    torch.cuda.synchronize()
+    _check(y0[None], Ws[0], masks[0], xs[0])
+    _check(y1[None], Ws[1], masks[1], xs[1])
+    ref0, ref1 = y0.clone(), y1.clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            nm.nm_spmv_group(mats, [xs[0][0]] * 2, [y0, y1])
+    for _ in range(2):
+        y0.fill_(float("nan"))
+        y1.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y0, ref0) and torch.equal(y1, ref1)
+
+
 def test_device_error_word_is_clear():
     assert nm.nm_device_errors(clear=False) == 0
     assert nm.nm_device_errors(clear=True) == 0
@@ -156,6 +227,20 @@ for (rows, K, N, M, B) in json.loads(sys.argv[2]):
     ok = oracle.within_tolerance(y.double().cpu().numpy(), yr, sr)
     if not ok.all():
         fails.append([rows, K, N, M, B, int((~ok).sum())])
+# a fused group of three matrices sharing x
+K, N, M = 4096, 2, 4
+Ws = [nm_synth.weights(r, K, r, "cuda") for r in (300, 100, 57)]
+ms = [nm_synth.topn_mask(W, N, M) for W in Ws]
+As = [nm.nm_pack(W, m, N, M) for W, m in zip(Ws, ms)]
+x = nm_synth.activations(K, 1, 9, True, "cuda")
+ys = nm.nm_spmv_group(As, [x[0]] * 3, y_dtype=torch.float32)
+torch.cuda.synchronize()
+for W, m, y in zip(Ws, ms, ys):
+    yr, sr = oracle.spmv_dense(W.cpu().numpy().view(np.uint16), m.cpu().numpy(),
+                               x.cpu().numpy().view(np.uint16))
+    ok = oracle.within_tolerance(y.double().cpu().numpy()[None], yr, sr)
+    if not ok.all():
+        fails.append(["group", W.shape[0], int((~ok).sum())])
 errs = nm.nm_device_errors()
 print(json.dumps({"fails": fails, "errors": errs}))
 """
