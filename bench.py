@@ -186,7 +186,13 @@ def max_over_ranks(value: float, world: int) -> float:
 
 
 def layer_list(wl):
-    return list(wl.all_layers()) if wl.blocks == 1 else list(wl.all_layers())[:7]
+    """Every layer of the workload's step (all blocks of a layer stream)."""
+    return list(wl.all_layers())
+
+
+def workload_bytes(wl, N, M, batch):
+    return sum(layer.rows * (layer.K // M) * N * 2 + layer.rows * layer.K // 8
+               + batch * layer.K * 2 + batch * layer.rows * 2 for _, layer in layer_list(wl))
 
 
 # ------------------------------------------------------------------ workload
@@ -374,12 +380,13 @@ def e2e_pass(layers, streams, copies, steps, warmup, batch):
 
 # ------------------------------------------------------------------ oracle leg
 
-def oracle_sample(wl, N, M, batch, row_fraction, device):
+def oracle_sample(wl, N, M, batch, row_fraction, device, max_layers=None):
     """Host copies for the oracle: the first ceil(rows * fraction) rows of
-    every layer of one step, packed by the oracle itself."""
+    every layer of one step (or of its first max_layers layers), packed by
+    the oracle itself."""
     import oracle
     sample = []
-    for li, layer in layer_list(wl):
+    for li, layer in layer_list(wl)[:max_layers]:
         W, mask, x = nm_synth.layer_inputs(wl, li, layer, N, M, batch, device)
         r = max(1, int(round(layer.rows * row_fraction)))
         Wn = W[:r].cpu().numpy()
@@ -459,9 +466,13 @@ def run_reference(args, world, rank):
     N, M = map(int, (args.pattern or "%d:%d" % wl.patterns[0]).split(":"))
     device = "cuda" if torch.cuda.is_available() else "cpu"
     threads = min(host_cores(), 64)
-    # each step: 1/32 of the rows of every layer of the step (a bounded sample)
-    frac = 1.0 / 32
-    sample = oracle_sample(wl, N, M, args.batch, frac, device)
+    # each step: a bounded sample, the first rows of every layer of the first
+    # block, about 16 MB of packed weights (a few ms to tens of ms of CPU work)
+    blk = len(wl.layers)
+    blk_bytes = sum(layer.rows * (layer.K // M) * N * 2 + layer.rows * layer.K // 8
+                    for _, layer in layer_list(wl)[:blk])
+    frac = min(1.0, 16e6 / blk_bytes)
+    sample = oracle_sample(wl, N, M, args.batch, frac, device, max_layers=blk)
     for _ in range(args.warmup):
         run_oracle(sample, N, M, threads)
     tot_t, tot_b = 0.0, 0
@@ -477,7 +488,9 @@ def run_reference(args, world, rank):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": config_block(args, wl, N, M, 0, desc),
            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                            "sample": "first 1/32 of the rows of each layer per step"},
+                            "sample": "per step: the first %.3g of the rows of each of the "
+                                      "first %d layers, row ranges over %d host threads, fp64"
+                                      % (frac, blk, threads)},
            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -488,7 +501,10 @@ def run_ours(args, world, rank, local):
     nmbuild.build()
     wl = nm_synth.WORKLOADS[args.workload]
     N, M = map(int, (args.pattern or "%d:%d" % wl.patterns[0]).split(":"))
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     copies = max(1, args.copies)
+    if workload_bytes(wl, N, M, args.batch) > 3 * l2:
+        copies = 1  # one step already streams more than 3x L2
     layers = build_workload(wl, N, M, args.batch, copies, keep_dense=not args.no_dense)
     bytes_per_call = step_bytes(layers, args.batch)
     step_b = sum(bytes_per_call)
@@ -509,8 +525,9 @@ def run_ours(args, world, rank, local):
     odt = max_over_ranks(odt, world)
 
     # each layer alone, L2-cold, for the per-layer figures
-    l2_bytes = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
-    layer_t = layer_pass(layers, args.batch, args.profile_steps, l2_bytes)
+    l2_bytes = l2
+    first_block = layers[:len(wl.layers)]
+    layer_t = layer_pass(first_block, args.batch, args.profile_steps, l2_bytes)
 
     dense = None
     if not args.no_dense:
@@ -535,11 +552,17 @@ def run_ours(args, world, rank, local):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         threads = min(host_cores(), 64)
-        sample = oracle_sample(wl, N, M, args.batch, 1.0, "cuda")
+        # a bounded sample: about 300 MB of packed weights (the whole step
+        # when it is smaller), the first rows of every layer of the first block
+        blk = len(wl.layers)
+        blk_bytes = sum(bytes_per_call[:blk])
+        frac = min(1.0, 3e8 / blk_bytes)
+        sample = oracle_sample(wl, N, M, args.batch, frac, "cuda", max_layers=blk)
         odt, ob = run_oracle(sample, N, M, threads)
         cpu = {"value": ob / odt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": "one full step (all rows of the %d layers), row ranges over %d host "
-                         "threads, fp64" % (len(layers), threads),
+               "sample": "%s of the rows of the first %d layers of the step, row ranges over "
+                         "%d host threads, fp64" % ("all" if frac >= 1 else "%.3g" % frac, blk,
+                                                    threads),
                "seconds": odt}
 
     if rank != 0:
@@ -548,7 +571,7 @@ def run_ours(args, world, rank, local):
     value = world * step_b * args.steps / dt / 1e9
     achieved = step_b * args.steps / dt / 1e9  # this rank's step: all launches are the SpMV kernel
     per_layer = {}
-    for L, b, lt in zip(layers, bytes_per_call, layer_t):
+    for L, b, lt in zip(first_block, bytes_per_call, layer_t):
         per_layer[L["name"]] = {"rows": L["rows"], "K": L["K"], "bytes": b, "us": lt * 1e6,
                                 "gbs": b / lt / 1e9, "frac_of_peak": b / lt / 1e9 / peak}
     out = {

@@ -1,4 +1,5 @@
-// Vectorised N:M SpMV kernel for sm_103a.
+// Vectorised N:M SpMV kernel (direct loads) and the mask-decode patterns
+// shared by every vectorised kernel, for sm_103a.
 //
 // The operation is the N:M sparse matrix-vector product with bitmask
 // indexing and fixed-step traversal of "SparseDecoding: Decoding-Aware
@@ -19,10 +20,14 @@
 //   * Rows are processed R at a time: all R*CPL chunk loads (16 B values +
 //     CK/8 B of mask) are issued before any is used, giving each thread
 //     R*CPL independent 16-byte loads in flight.
-//   * Mask decode in registers: the positions of a group's set bits come
-//     from find-first-set / find-last-set, and a byte permute gathers the
-//     matching fp16 x lanes into a half2 next to the value pair.  Products
-//     use fp16 x fp16 -> fp32 FMA.
+//   * Mask decode in registers (Pattern<N, M> below: byte-permute lookup
+//     tables for 2:4 and 1:4, one find-leading-one per kept position for the
+//     8-wide patterns), and a byte permute gathers the matching fp16 x lanes
+//     into a half2 next to the value pair.  Products use fp16 x fp16 -> fp32
+//     FMA.
+// This kernel loads with plain 128-bit loads and is the path for K not a
+// multiple of 128; the bulk-staged kernels (nm_rows.cuh, nm_bulk.cuh) take
+// the other shapes.
 //   * Each warp reduces its R*B partial sums with a reduce-scatter butterfly
 //     (V-1 shuffles for V sums), warps combine through shared memory, and
 //     the totals are rounded once into y (or carried to the next K tile in

@@ -83,16 +83,6 @@ struct RowsArgs {
 
 constexpr int kRowsMaxWarps = 16;
 
-// Where task j of warp w lives: K tile and row tile.
-struct RowsTask {
-    int kt, rt;
-};
-__device__ __forceinline__ RowsTask rows_task(int j, int w, int W, int per_kt)
-{
-    const int kt = j / per_kt;
-    return RowsTask{kt, w + (j - kt * per_kt) * W};
-}
-
 template <int R, int MB>
 __device__ __forceinline__ void rows_issue(const RowsArgs &a, const uint8_t *values,
                                            const uint8_t *masks, uint8_t *st, uint64_t *bar,
@@ -183,22 +173,30 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     }
 
     // Prefetch this warp's first SW tasks (weights only: no dependence on
-    // the previous kernel).
+    // the previous kernel).  The issue cursor (K tile, index within it) and
+    // the consume cursor (slot, phase) advance by one task at a time.
     int issued = 0;
+    int iss_kt = 0, iss_n = 0;
     if (lane == 0) {
         for (; issued < a.SW && issued < ntask; ++issued) {
-            const RowsTask t = rows_task(issued, warp, W, per_kt);
+            const int rt = warp + iss_n * W;
             rows_issue<R, MB>(a, mt.values, mt.masks,
                               my_ring + static_cast<size_t>(issued) * a.stage_bytes,
-                              &my_full[issued], t.kt, t.rt * R, min(R, r_count - t.rt * R),
+                              &my_full[issued], iss_kt, rt * R, min(R, r_count - rt * R),
                               r_begin, pol);
+            if (++iss_n == per_kt) {
+                iss_n = 0;
+                ++iss_kt;
+            }
         }
     }
 
     pdl_wait();  // x may be the previous kernel's output; y may still be read by it
 
     bool failed = false;
-    int j = 0;  // next task of this warp
+    int j = 0;          // next task of this warp
+    int slot = 0;       // its slot (j % SW)
+    uint32_t phase = 0; // parity of its slot's phase ((j / SW) & 1)
     for (int kt = 0; kt < a.ktiles; ++kt) {
         const int c0 = kt * a.tile_chunks;
         const int nc = min(a.tile_chunks, a.chunks - c0);
@@ -218,11 +216,10 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
         named_barrier_sync(1, blockDim.x);
 
         for (int n = 0; n < per_kt; ++n, ++j) {
-            const int slot = j % a.SW;
             const int rt = warp + n * W;
             const int i0 = rt * R;
             const int nr = min(R, r_count - i0);
-            if (!failed && !mbar_wait(&my_full[slot], (j / a.SW) & 1)) {
+            if (!failed && !mbar_wait(&my_full[slot], phase)) {
                 failed = true;  // give up waiting; y is garbage, the error word says so
                 atomicOr(a.err, kDevErrPipeTimeout);
             }
@@ -264,10 +261,18 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
             __syncwarp();
             if (lane == 0 && issued < ntask && !failed) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                const RowsTask t = rows_task(issued, warp, W, per_kt);
-                rows_issue<R, MB>(a, mt.values, mt.masks, sv, &my_full[slot], t.kt, t.rt * R,
-                                  min(R, r_count - t.rt * R), r_begin, pol);
+                const int irt = warp + iss_n * W;
+                rows_issue<R, MB>(a, mt.values, mt.masks, sv, &my_full[slot], iss_kt, irt * R,
+                                  min(R, r_count - irt * R), r_begin, pol);
                 ++issued;
+                if (++iss_n == per_kt) {
+                    iss_n = 0;
+                    ++iss_kt;
+                }
+            }
+            if (++slot == a.SW) {
+                slot = 0;
+                phase ^= 1u;
             }
 
             warp_reduce_scatter<V>(acc, lane);
