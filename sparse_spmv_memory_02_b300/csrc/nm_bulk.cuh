@@ -265,14 +265,16 @@ struct BulkTuning {
     int rows_R = 0;                // rows per task (0: chosen)
     int rows_task_bytes = 6144;    // largest task (rows x K tile) in bytes
     int rows_ring_bytes = 200000;  // shared memory for the slots
-    int rows_max_seg = 32768;      // longest row segment before K is tiled
-    int l2_prefetch_bytes = 0;     // weights warmed in L2 at CTA start (0: off)
+    int rows_xtile_bytes = 49152;  // largest x tile (B vectors) before K is tiled
+    int rows_pair = 0;             // size each CTA to half an SM (see nm_rows.cuh)
+    int rows_pre = 1;              // tasks per warp copied before the dependence wait (<= SW)
+    int rows_l2pre_bytes = 0;      // weight bytes per CTA warmed in L2 before that wait
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
-// rows_ring, rows_seg, rows (row-per-warp kernel), ctas, pdl, l2pf (both);
-// read once per process.
+// rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows (row-per-warp kernel), ctas, pdl
+// (both); read once per process.
 const BulkTuning &bulk_tuning();
 
 struct BulkPlan {

@@ -38,11 +38,13 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "pdl") && (v == 0 || v == 1)) t.pdl = v;
         else if (!std::strcmp(tok, "rows_warps") && v >= 1 && v <= kRowsMaxWarps) t.rows_warps = v;
         else if (!std::strcmp(tok, "rows_R") && (v == 1 || v == 2 || v == 4)) t.rows_R = v;
-        else if (!std::strcmp(tok, "rows_task") && v >= 1024) t.rows_task_bytes = v;
+        else if (!std::strcmp(tok, "rows_task") && v >= 512) t.rows_task_bytes = v;
         else if (!std::strcmp(tok, "rows_ring") && v >= 4096) t.rows_ring_bytes = v;
-        else if (!std::strcmp(tok, "rows_seg") && v >= 1024) t.rows_max_seg = v;
+        else if (!std::strcmp(tok, "rows_xtile") && v >= 1024) t.rows_xtile_bytes = v;
         else if (!std::strcmp(tok, "rows") && (v == 0 || v == 1)) t.rows_kernel = v;
-        else if (!std::strcmp(tok, "l2pf") && v >= 0) t.l2_prefetch_bytes = v / 16 * 16;
+        else if (!std::strcmp(tok, "rows_pair") && (v == 0 || v == 1)) t.rows_pair = v;
+        else if (!std::strcmp(tok, "rows_pre") && v >= 0 && v <= 8) t.rows_pre = v;
+        else if (!std::strcmp(tok, "rows_l2pre") && v >= 0) t.rows_l2pre_bytes = v;
     }
     return t;
 }
@@ -71,6 +73,35 @@ int max_dynamic_smem()
         return -1;
     if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
     return v;
+}
+
+bool rows_pair_limits(int *smem_per_cta, int *regs_per_cta)
+{
+    static std::atomic<int> smem_cache[64], regs_cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+    if (dev < 64 && smem_cache[dev].load(std::memory_order_acquire) > 0) {
+        *smem_per_cta = smem_cache[dev].load(std::memory_order_relaxed);
+        *regs_per_cta = regs_cache[dev].load(std::memory_order_relaxed);
+        return true;
+    }
+    int per_sm = 0, reserved = 0, regs = 0;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev) !=
+            cudaSuccess)
+        return false;
+    const int smem = per_sm / 2 - reserved;
+    if (smem <= 0 || regs <= 0) return false;
+    if (dev < 64) {
+        regs_cache[dev].store(regs / 2, std::memory_order_relaxed);
+        smem_cache[dev].store(smem, std::memory_order_release);
+    }
+    *smem_per_cta = smem;
+    *regs_per_cta = regs / 2;
+    return true;
 }
 
 bool bulk_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, BulkPlan *out)
@@ -153,58 +184,68 @@ namespace {
 // The row kernel's plan for a K (in chunks), batch and a grid whose busiest
 // CTA has rows_per_cta rows.
 bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, int max_smem,
-                    RowsPlan *out)
+                    int max_warps, RowsPlan *out)
 {
     const BulkTuning &t = bulk_tuning();
     const int MB = CK / 8;  // mask bytes per chunk
-    const int W = t.rows_warps ? t.rows_warps : 16;
-    const int64_t row_bytes = static_cast<int64_t>(chunks) * (16 + MB);
+    const int W = std::min(t.rows_warps ? t.rows_warps : kRowsMaxWarps, max_warps);
+    if (W < 1) return false;
+
+    // 1. K tile: the x all warps share, B * tile * CK * 2 bytes; all of K
+    //    unless that exceeds rows_xtile bytes, else even tiles of a multiple
+    //    of 32 chunks (two buffers, and the rows' partial sums carried).
+    RowsPlan p;
+    p.W = W;
+    p.grid = grid;
     const int64_t x_bytes = static_cast<int64_t>(B) * chunks * CK * 2;
+    int64_t kt = std::max<int64_t>(1, (x_bytes + t.rows_xtile_bytes - 1) / t.rows_xtile_bytes);
+    int64_t tile = (chunks + kt - 1) / kt;
+    if (kt > 1) tile = (tile + 31) / 32 * 32;
+    if (tile >= chunks) tile = chunks;
+    p.tile_chunks = static_cast<int>(tile);
+    p.ktiles = static_cast<int>((chunks + tile - 1) / tile);
+    const int last_chunks = chunks - (p.ktiles - 1) * p.tile_chunks;
+    p.xbuf_bytes = B * (CK / 8) * p.tile_chunks * 16;
+    const int nxb = p.ktiles > 1 ? 2 : 1;
+    const int64_t carry64 = p.ktiles > 1 ? rows_per_cta * B * 4 : 0;
+    if (carry64 > 64 * 1024) return false;
+    const int carry = static_cast<int>(carry64);
 
-    // Every warp owns SW >= 2 slots of one task each; a task is R rows x one
-    // K tile of at most `target` bytes, rows longer than that are split into
-    // K tiles.  Smaller tasks are tried until everything fits.
-    for (int target = t.rows_task_bytes; target >= 1024; target /= 2) {
-        RowsPlan p;
-        p.W = W;
-        p.grid = grid;
-        // 1. K tile: whole rows if a row fits the task and the x tile 48 KB;
-        //    tiles are multiples of 32 chunks and split the row evenly.
-        const int64_t seg_cap = std::min<int64_t>(target, t.rows_max_seg);
-        int64_t kt = std::max<int64_t>((row_bytes + seg_cap - 1) / seg_cap,
-                                       (x_bytes + 48 * 1024 - 1) / (48 * 1024));
-        kt = std::max<int64_t>(1, kt);
-        int64_t tile = (chunks + kt - 1) / kt;
-        tile = (tile + 31) / 32 * 32;
-        if (tile > chunks) tile = chunks;  // one tile: exactly the row
-        p.tile_chunks = static_cast<int>(tile);
-        p.ktiles = static_cast<int>((chunks + tile - 1) / tile);
-        p.seg_v = p.tile_chunks * 16;
-        p.seg_m = round_up(p.tile_chunks * MB, 16);
-        const int seg = p.seg_v + p.seg_m;
+    // 2. Tasks: R rows x one segment of a K tile, at most `target` bytes; a
+    //    tile row longer than that is cut into even segments of a multiple
+    //    of 32 chunks.  Smaller tasks are tried until everything fits with
+    //    at least two slots per warp.
+    for (int target = t.rows_task_bytes; target >= 512; target /= 2) {
+        const int64_t tile_bytes = static_cast<int64_t>(p.tile_chunks) * (16 + MB);
+        int64_t nseg = std::max<int64_t>(1, (tile_bytes + target - 1) / target);
+        int64_t seg = (p.tile_chunks + nseg - 1) / nseg;
+        if (nseg > 1) seg = (seg + 31) / 32 * 32;
+        if (seg >= p.tile_chunks) seg = p.tile_chunks;
+        p.seg_chunks = static_cast<int>(seg);
+        p.nseg = static_cast<int>((p.tile_chunks + seg - 1) / seg);
+        p.nseg_last = static_cast<int>((last_chunks + seg - 1) / seg);
+        p.seg_v = p.seg_chunks * 16;
+        p.seg_m = round_up(p.seg_chunks * MB, 16);
+        const int segb = p.seg_v + p.seg_m;
 
-        // 2. Rows per task: the largest of 1, 2, 4 with R * seg <= target
-        //    (R * B partial sums per lane stay <= 8).
+        // Rows per task: the largest of 1, 2, 4 with R * segb <= target
+        // (R * B partial sums per lane stay <= 8), whole tile rows only.
         int R = 1;
-        if (t.rows_R) R = t.rows_R;
+        if (t.rows_R) R = p.nseg == 1 ? t.rows_R : 1;
         else
-            while (R < 4 && 2 * R * seg <= target && 2 * R * B <= 8) R *= 2;
+            while (p.nseg == 1 && R < 4 && 2 * R * segb <= target && 2 * R * B <= 8) R *= 2;
         if (R * B > 8) return false;
         p.R = R;
-        p.stage_bytes = R * seg;
+        p.stage_bytes = R * segb;
 
-        // 3. Shared memory: slots [W][SW] | x buffers | barriers | carry.
-        const int64_t carry64 = p.ktiles > 1 ? rows_per_cta * B * 4 : 0;
-        if (carry64 > 64 * 1024) return false;
-        const int carry = static_cast<int>(carry64);
-        p.xbuf_bytes = B * (CK / 8) * p.tile_chunks * 16;
-        const int nxb = p.ktiles > 1 ? 2 : 1;
-        int SW = std::max(2, std::min(4, t.rows_ring_bytes / (W * p.stage_bytes)));
+        // 3. Shared memory: slots [W][SW] | x buffers | barriers | carry;
+        //    SW from 2 to 4, as many as the ring budget and max_smem allow.
         auto total = [&](int sw) {
             const size_t S = static_cast<size_t>(sw) * W;
             return S * p.stage_bytes + static_cast<size_t>(nxb) * p.xbuf_bytes +
                    round_up(static_cast<int>(8 * S), 16) + carry;
         };
+        int SW = std::max(2, std::min(4, t.rows_ring_bytes / (W * p.stage_bytes)));
         while (SW > 2 && total(SW) > static_cast<size_t>(max_smem)) --SW;
         if (total(SW) > static_cast<size_t>(max_smem)) continue;
         const int S = SW * W;
@@ -221,7 +262,8 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
 
 }  // namespace
 
-bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, RowsPlan *out)
+bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
+               RowsPlan *out)
 {
     if (rows <= 0 || chunks <= 0 || B < 1 || B > 2) return false;
     const BulkTuning &t = bulk_tuning();
@@ -233,11 +275,11 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, R
     grid = std::max<int64_t>(grid, (rows + max_rows - 1) / max_rows);
     if (grid > 0x7fffffff) return false;
     return rows_plan_impl((rows + grid - 1) / grid, static_cast<int>(grid), chunks, CK, B,
-                          max_smem, out);
+                          max_smem, max_warps, out);
 }
 
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
-                     int max_smem, RowsPlan *out, int *cta_begin)
+                     int max_smem, int max_warps, RowsPlan *out, int *cta_begin)
 {
     if (count < 1 || count > kRowsMaxGroup || chunks <= 0 || B < 1 || B > 2) return false;
     const BulkTuning &t = bulk_tuning();
@@ -283,7 +325,7 @@ bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, 
         rpc = std::max<int64_t>(rpc, (rows[i] + g[i] - 1) / g[i]);
         cta_begin[i + 1] = cta_begin[i] + g[i];
     }
-    return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, out);
+    return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, max_warps, out);
 }
 
 }  // namespace nm

@@ -105,7 +105,8 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
 }
 
 // Ask L2 to fetch `bytes` (a multiple of 16, 16-byte aligned address) from
-// HBM now; nothing waits for it.  Later reads of the range hit L2.
+// HBM now; nothing waits for it and no data comes back to the SM.  Later
+// reads of the range hit L2.
 __device__ __forceinline__ void prefetch_l2(const void *src_gmem, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes)

@@ -9,41 +9,58 @@
 // value and mask bit is read from HBM once, so the kernel's job is to keep
 // enough bytes in flight with as few instructions per byte as possible.
 //
-// Work split.  Rows are split evenly over one CTA per SM.  A CTA's rows form
-// row tiles of R rows; with K split into K tiles (usually one), a task is
-// one row tile x one K tile, and task (kt, rt) belongs to warp rt % W.
+// Work split.  Rows are split evenly over one CTA per SM.  x is held in
+// shared memory for all of K when B * K * 2 bytes fit the x budget (else K
+// is cut into K tiles, each staged in turn).  A CTA's rows form row tiles of
+// R rows; a task is one row tile x one segment of the K tile (a row longer
+// than the task size is cut into even segments of a multiple of 32 chunks),
+// and row tile rt belongs to warp rt % W, which takes its segments in order
+// and keeps the row's sums in registers across them.
 //
 // Self-feeding warps.  Warp w owns SW shared-memory slots.  Its lane 0
-// issues the bulk copies of w's own next SW tasks (the R rows' value
-// segments and mask segments; with a single K tile the R rows are one
-// contiguous byte range of each array -- a packed row is exactly K/M*N
-// values and K/32 mask words -- so a task is two copies), each completing on
-// the slot's mbarrier.  After the warp has read a slot it immediately issues
-// its task SW ahead into it.  Every warp is thus its own pipeline with SW-1
-// tasks in flight: bulk copies issued by one warp complete at a limited rate
-// per warp on this GPU, and W independent issuers per SM are what reach HBM
+// issues the bulk copies of w's own next tasks (the rows' value segments and
+// mask segments; a segment of one row, or R whole rows, is one contiguous
+// byte range of each array -- a packed row is exactly K/M*N values and K/32
+// mask words -- so a task is two copies), each completing on the slot's
+// mbarrier.  After the warp has read a slot it immediately issues its task
+// SW ahead into it.  Every warp is thus its own pipeline with up to SW tasks
+// in flight: bulk copies issued by one warp complete at a limited rate per
+// warp on this GPU, and W independent issuers per SM are what reach HBM
 // bandwidth.  There is no producer warp, no "empty" barrier and no
 // synchronisation between warps other than one named barrier per K tile.
 // A warp waits on every phase of its own slots in order, so a parity wait
 // can never mistake an older phase for the one it wants.
 //
-// Per task, lane l walks the chunk columns l, l+32, ... of the K tile: it
-// loads the column's x units from shared memory once and uses them for all R
-// rows (each a 16-byte value chunk plus its mask bits, decoded by byte
-// permutes in Pattern<N, M>), accumulating in fp32; the warp reduces its R*B
-// sums with a reduce-scatter butterfly and one lane per sum rounds it into y
-// (or adds it to the row's carry when the row spans several K tiles; a row's
-// tiles always go to the same warp).
+// Per task, lane l walks the segment's chunk columns l, l+32, ...: it loads
+// the column's x units from shared memory once and uses them for all R rows
+// (each a 16-byte value chunk plus its mask bits, decoded by byte permutes
+// in Pattern<N, M>), accumulating in fp32; after a row tile's last segment
+// the warp reduces its R*B sums with a reduce-scatter butterfly and one lane
+// per sum rounds it into y (or adds it to the row's carry when the row spans
+// several K tiles; a row's tiles always go to the same warp).
 //
-// Programmatic dependent launch: the first SW tasks of every warp are issued
-// before griddepcontrol.wait -- the packed weights are read-only input that
-// no kernel of this library writes -- so one call's weight stream starts
-// under the tail of the previous call; x is read and y written only after
-// the wait.
+// Programmatic dependent launch: the packed weights are read-only input that
+// no kernel of this library writes, so each warp issues its first `pre`
+// tasks (one by default) before griddepcontrol.wait and one call's weight
+// stream starts under the tail of the previous call; x is read and y written
+// only after the wait.  The rest of the first SW tasks is issued once x is
+// loaded: the x loads are L2 hits, and copies issued earlier by the same SM
+// would be served ahead of them, so a deep prefetch before the wait delays
+// the start of compute by more than it saves.  The prologue before the
+// first copies is kept short (barriers initialised by one thread each, the
+// CTA's rows looked up before the barrier setup) because a CTA of the next
+// call only starts when the SM's CTA of the previous call exits.
+//
+// Two options measured slower on the Llama-3.1-8B-shaped block and are off
+// by default: warming L2 with the CTA's next rows before the wait
+// (rows_l2pre), and planning each launch for half an SM (rows_pair) so that
+// CTAs of consecutive calls share SMs -- half the shared memory per CTA
+// leaves too few bytes in flight once a call runs alone.
 #pragma once
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "nm_bulk.cuh"  // Pattern<N, M>, pipeline primitives, tuning
@@ -60,46 +77,58 @@ struct RowsMat {
     const __half *x;        // [B][ldx]
     void *y;                // [B][ldy]
     int64_t ldy;
-    int cta_begin;          // first CTA of this matrix
     int row_base, row_extra;  // its CTA c owns row_base rows (+1 if c < row_extra)
 };
 
+// The scalars every CTA reads first come first (kernel parameters are read
+// through the constant cache; keeping them on few lines keeps the prologue
+// short), the per-matrix table last.
 struct RowsArgs {
-    RowsMat mat[kRowsMaxGroup];
     int nmat;
-    unsigned int *err;      // device error word
-    int64_t ldx, vrow_bytes, mrow_bytes;
-    int chunks;             // 16-byte value chunks per row
-    int tile_chunks;        // chunks per K tile
-    int ktiles;
     int SW;                 // slots per warp
+    int pre;                // tasks per warp issued before the dependence wait (<= SW)
+    int chunks;             // 16-byte value chunks per row
+    int tile_chunks;        // chunks per K tile (the x held in shared memory at once)
+    int ktiles;
+    int seg_chunks;         // chunks per row segment (one task) within a K tile
+    int nseg, nseg_last;    // segments of a full K tile / of the last K tile
     int seg_v, seg_m;       // shared bytes of one row's value / mask segment
     int stage_bytes;        // R * (seg_v + seg_m)
     int xbuf_bytes;         // one x tile buffer: B * XV * tile_chunks * 16
     int off_x, off_bar, off_carry;
     int y_f32;
-    int pf_bytes;           // bytes of values (and matching masks) warmed in L2 per CTA
+    int l2pre_rows;         // rows per CTA warmed in L2 before the dependence wait
+    int cta_begin[kRowsMaxGroup + 1];  // first CTA of each matrix; [nmat] = grid
+    int64_t ldx, vrow_bytes, mrow_bytes;
+    unsigned int *err;      // device error word
+    RowsMat mat[kRowsMaxGroup];
 };
 
 constexpr int kRowsMaxWarps = 16;
 
+// Copies task (K tile kt, segment sg, rows i0 .. i0+nr-1 of the CTA) into a
+// slot: the rows' value segments at st + i * seg_v, their mask segments at
+// st + R * seg_v + i * seg_m, completing on bar.
 template <int R, int MB>
 __device__ __forceinline__ void rows_issue(const RowsArgs &a, const uint8_t *values,
                                            const uint8_t *masks, uint8_t *st, uint64_t *bar,
-                                           int kt, int i0, int nr, int r_begin, uint64_t pol)
+                                           int kt, int sg, int i0, int nr, int r_begin,
+                                           uint64_t pol)
 {
-    const int c0 = kt * a.tile_chunks;
-    const int nc = min(a.tile_chunks, a.chunks - c0);
+    const int t0 = kt * a.tile_chunks;
+    const int c0 = t0 + sg * a.seg_chunks;
+    const int nc = min(a.seg_chunks, min(a.tile_chunks, a.chunks - t0) - sg * a.seg_chunks);
     const uint32_t vb = static_cast<uint32_t>(nc) * 16u;
     const uint32_t mb = static_cast<uint32_t>(nc) * MB;
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * (vb + mb));
     const int64_t row0 = r_begin + i0;
-    if (a.ktiles == 1) {
-        // whole rows: seg_v == vrow_bytes and seg_m == mrow_bytes, so the
-        // rows are one contiguous range of each array, in the slot's layout
-        bulk_g2s(st, values + row0 * a.vrow_bytes, static_cast<uint32_t>(nr) * vb, bar, pol);
-        bulk_g2s(st + R * a.seg_v, masks + row0 * a.mrow_bytes, static_cast<uint32_t>(nr) * mb,
+    if (R == 1 || a.seg_chunks == a.chunks) {
+        // one row, or whole rows (then seg_v == vrow_bytes and seg_m ==
+        // mrow_bytes): one contiguous range of each array, in the slot's layout
+        bulk_g2s(st, values + row0 * a.vrow_bytes + c0 * 16LL, static_cast<uint32_t>(nr) * vb,
                  bar, pol);
+        bulk_g2s(st + R * a.seg_v, masks + row0 * a.mrow_bytes + static_cast<int64_t>(c0) * MB,
+                 static_cast<uint32_t>(nr) * mb, bar, pol);
     } else {
         for (int i = 0; i < nr; ++i) {
             const int64_t row = row0 + i;
@@ -132,63 +161,71 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     uint64_t *full = reinterpret_cast<uint64_t *>(rows_smem + a.off_bar);  // [W][SW]
     float *carry = reinterpret_cast<float *>(rows_smem + a.off_carry);     // [rows of CTA][B]
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < W * a.SW; ++s) mbar_init(&full[s], 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
     pdl_launch_dependents();
 
     // The matrix this CTA works on, and its rows of it.
     int mi = 0;
-    while (mi + 1 < a.nmat && static_cast<int>(blockIdx.x) >= a.mat[mi + 1].cta_begin) ++mi;
+    while (mi + 1 < a.nmat && static_cast<int>(blockIdx.x) >= a.cta_begin[mi + 1]) ++mi;
     const RowsMat &mt = a.mat[mi];
-    const int cta = static_cast<int>(blockIdx.x) - mt.cta_begin;
+    const int cta = static_cast<int>(blockIdx.x) - a.cta_begin[mi];
     const int r_begin = cta * mt.row_base + min(cta, mt.row_extra);
     const int r_count = mt.row_base + (cta < mt.row_extra ? 1 : 0);
     const int nrt = (r_count + R - 1) / R;                         // row tiles of the CTA
     const int per_kt = nrt > warp ? (nrt - warp + W - 1) / W : 0;  // this warp's tiles per K tile
-    const int ntask = per_kt * a.ktiles;
+    const int ntask = per_kt * ((a.ktiles - 1) * a.nseg + a.nseg_last);
     uint8_t *my_ring = ring + static_cast<size_t>(warp) * a.SW * a.stage_bytes;
     uint64_t *my_full = full + warp * a.SW;
     const uint64_t pol = l2_evict_first_policy();
 
-    // Warm L2 with the start of this CTA's weights (values and masks of its
-    // rows are two contiguous ranges) while the previous kernel finishes and
-    // x becomes readable: up to pf_bytes in pieces of up to 32 KB, one piece
-    // per lane of the last warp, so the first tasks' copies below and the
-    // refills after them hit L2 instead of waiting on HBM.
-    if (warp == W - 1 && a.pf_bytes > 0) {
-        const int64_t vtot = static_cast<int64_t>(r_count) * a.vrow_bytes;
-        const int64_t mtot = static_cast<int64_t>(r_count) * a.mrow_bytes;
-        const int64_t vlen = min(vtot, static_cast<int64_t>(a.pf_bytes));
-        const int64_t mlen = min(mtot, vlen / (a.vrow_bytes / a.mrow_bytes)) / 16 * 16;
-        const uint8_t *vsrc = mt.values + static_cast<int64_t>(r_begin) * a.vrow_bytes;
-        const uint8_t *msrc = mt.masks + static_cast<int64_t>(r_begin) * a.mrow_bytes;
-        constexpr int64_t kPiece = 32768;
-        for (int64_t off = static_cast<int64_t>(lane) * kPiece; off < vlen; off += 32 * kPiece)
-            prefetch_l2(vsrc + off, static_cast<uint32_t>(min(kPiece, vlen - off)));
-        for (int64_t off = static_cast<int64_t>(lane) * kPiece; off < mlen; off += 32 * kPiece)
-            prefetch_l2(msrc + off, static_cast<uint32_t>(min(kPiece, mlen - off)));
+    // Thread s initialises slot barrier s (all at once, not one thread
+    // looping over W * SW of them).
+    if (threadIdx.x < W * a.SW) {
+        mbar_init(&full[threadIdx.x], 1);
+        mbar_fence_init();
     }
+    __syncthreads();
 
-    // Prefetch this warp's first SW tasks (weights only: no dependence on
-    // the previous kernel).  The issue cursor (K tile, index within it) and
-    // the consume cursor (slot, phase) advance by one task at a time.
+    // Issue cursor over this warp's tasks in consumption order: K tile, then
+    // row tile, then segment.  It advances by one task at a time.
     int issued = 0;
-    int iss_kt = 0, iss_n = 0;
-    if (lane == 0) {
-        for (; issued < a.SW && issued < ntask; ++issued) {
-            const int rt = warp + iss_n * W;
-            rows_issue<R, MB>(a, mt.values, mt.masks,
-                              my_ring + static_cast<size_t>(issued) * a.stage_bytes,
-                              &my_full[issued], iss_kt, rt * R, min(R, r_count - rt * R),
-                              r_begin, pol);
+    int iss_kt = 0, iss_n = 0, iss_s = 0;
+    auto issue_next = [&](uint8_t *st, uint64_t *bar) {
+        const int rt = warp + iss_n * W;
+        rows_issue<R, MB>(a, mt.values, mt.masks, st, bar, iss_kt, iss_s, rt * R,
+                          min(R, r_count - rt * R), r_begin, pol);
+        ++issued;
+        if (++iss_s == (iss_kt == a.ktiles - 1 ? a.nseg_last : a.nseg)) {
+            iss_s = 0;
             if (++iss_n == per_kt) {
                 iss_n = 0;
                 ++iss_kt;
             }
         }
+    };
+
+    // This warp's first `pre` tasks (weights only: no dependence on the
+    // previous kernel); the rest of its first SW after x is staged.
+    if (lane == 0)
+        while (issued < a.pre && issued < ntask)
+            issue_next(my_ring + static_cast<size_t>(issued) * a.stage_bytes, &my_full[issued]);
+
+    // Warm L2 with the CTA's next rows (values and masks of consecutive rows
+    // are contiguous) in pieces of up to 32 KB, one piece per lane of the
+    // last warp: HBM streams them while the previous kernel drains, and no
+    // data comes back to the SM to queue ahead of the x loads below.  The
+    // rows the `pre` tasks copy are skipped.
+    if (a.l2pre_rows > 0 && warp == W - 1) {
+        const int skip = min(r_count, (a.pre + a.nseg - 1) / a.nseg * W * R);
+        const int n = min(r_count - skip, a.l2pre_rows);
+        const int64_t r0 = r_begin + skip;
+        const uint8_t *vsrc = mt.values + r0 * a.vrow_bytes;
+        const uint8_t *msrc = mt.masks + r0 * a.mrow_bytes;
+        const int64_t vlen = n * a.vrow_bytes, mlen = n * a.mrow_bytes;
+        constexpr int64_t kPiece = 32768;
+        for (int64_t off = lane * kPiece; off < vlen; off += 32 * kPiece)
+            prefetch_l2(vsrc + off, static_cast<uint32_t>(min(kPiece, vlen - off)));
+        for (int64_t off = lane * kPiece; off < mlen; off += 32 * kPiece)
+            prefetch_l2(msrc + off, static_cast<uint32_t>(min(kPiece, mlen - off)));
     }
 
     pdl_wait();  // x may be the previous kernel's output; y may still be read by it
@@ -200,79 +237,100 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     for (int kt = 0; kt < a.ktiles; ++kt) {
         const int c0 = kt * a.tile_chunks;
         const int nc = min(a.tile_chunks, a.chunks - c0);
+        const int nseg = kt == a.ktiles - 1 ? a.nseg_last : a.nseg;
         uint8_t *xs = xbuf + (kt & 1) * a.xbuf_bytes;
         // x tile -> shared memory, unit-major: unit u of chunk column c of
         // vector b at ((b * XV + u) * tile_chunks + c) * 16, so that a warp
         // reading one unit of 32 consecutive columns reads 512 contiguous
         // bytes.  The buffer written here was last read in K tile kt-2, and
         // every warp has passed the barrier of tile kt-1 since.
-        for (int e = threadIdx.x; e < B * XV * nc; e += blockDim.x) {
-            const int b = e / (XV * nc);
-            const int r = e - b * (XV * nc);
-            const int c = r / XV, u = r - (r / XV) * XV;
-            const uint4 t = ld_cg_v4(mt.x + b * a.ldx + static_cast<int64_t>(c0 + c) * CK + 8 * u);
-            *reinterpret_cast<uint4 *>(xs + ((b * XV + u) * a.tile_chunks + c) * 16) = t;
+        // Each thread issues up to XU loads before its first store, so a
+        // tile costs one memory round trip per XU * blockDim units.
+        constexpr int XU = 4;
+        const int xunits = B * XV * nc;
+        for (int e0 = threadIdx.x; e0 < xunits; e0 += XU * blockDim.x) {
+            uint4 t[XU];
+            int dst[XU];
+#pragma unroll
+            for (int q = 0; q < XU; ++q) {
+                const int e = e0 + q * static_cast<int>(blockDim.x);
+                if (e < xunits) {
+                    const int b = B == 1 ? 0 : e / (XV * nc);
+                    const int r = e - b * (XV * nc);
+                    const int c = r / XV, u = r - (r / XV) * XV;
+                    t[q] = ld_cg_v4(mt.x + b * a.ldx + static_cast<int64_t>(c0 + c) * CK + 8 * u);
+                    dst[q] = ((b * XV + u) * a.tile_chunks + c) * 16;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < XU; ++q)
+                if (e0 + q * static_cast<int>(blockDim.x) < xunits)
+                    *reinterpret_cast<uint4 *>(xs + dst[q]) = t[q];
         }
+        if (kt == 0 && lane == 0)
+            while (issued < a.SW && issued < ntask)
+                issue_next(my_ring + static_cast<size_t>(issued) * a.stage_bytes,
+                           &my_full[issued]);
         named_barrier_sync(1, blockDim.x);
 
-        for (int n = 0; n < per_kt; ++n, ++j) {
+        for (int n = 0; n < per_kt; ++n) {
             const int rt = warp + n * W;
             const int i0 = rt * R;
             const int nr = min(R, r_count - i0);
-            if (!failed && !mbar_wait(&my_full[slot], phase)) {
-                failed = true;  // give up waiting; y is garbage, the error word says so
-                atomicOr(a.err, kDevErrPipeTimeout);
-            }
-            uint8_t *sv = my_ring + static_cast<size_t>(slot) * a.stage_bytes;
-            const uint8_t *sm = sv + R * a.seg_v;
-
             float acc[V];
 #pragma unroll
             for (int t = 0; t < V; ++t) acc[t] = 0.f;
+            for (int sg = 0; sg < nseg; ++sg, ++j) {
+                if (!failed && !mbar_wait(&my_full[slot], phase)) {
+                    failed = true;  // give up waiting; y is garbage, the error word says so
+                    atomicOr(a.err, kDevErrPipeTimeout);
+                }
+                uint8_t *sv = my_ring + static_cast<size_t>(slot) * a.stage_bytes;
+                const uint8_t *sm = sv + R * a.seg_v;
+                // columns [cs, ce) of the K tile; the slot holds them from 0
+                const int cs = sg * a.seg_chunks;
+                const int ce = min(nc, cs + a.seg_chunks);
+                const uint8_t *xseg = xs + cs * 16;
 #pragma unroll 2
-            for (int c = lane; c < nc; c += 32) {
-                uint32_t xw[B][XR];
+                for (int c = lane; c < ce - cs; c += 32) {
+                    uint32_t xw[B][XR];
 #pragma unroll
-                for (int b = 0; b < B; ++b)
+                    for (int b = 0; b < B; ++b)
 #pragma unroll
-                    for (int u = 0; u < XV; ++u) {
-                        const uint4 t = *reinterpret_cast<const uint4 *>(
-                            xs + ((b * XV + u) * a.tile_chunks + c) * 16);
-                        xw[b][4 * u + 0] = t.x;
-                        xw[b][4 * u + 1] = t.y;
-                        xw[b][4 * u + 2] = t.z;
-                        xw[b][4 * u + 3] = t.w;
-                    }
+                        for (int u = 0; u < XV; ++u) {
+                            const uint4 t = *reinterpret_cast<const uint4 *>(
+                                xseg + ((b * XV + u) * a.tile_chunks + c) * 16);
+                            xw[b][4 * u + 0] = t.x;
+                            xw[b][4 * u + 1] = t.y;
+                            xw[b][4 * u + 2] = t.z;
+                            xw[b][4 * u + 3] = t.w;
+                        }
 #pragma unroll
-                for (int i = 0; i < R; ++i) {
-                    if (i < nr) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
-                        const mask_t m = *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
-                        const typename P::Sel sel = P::decode(m);
+                    for (int i = 0; i < R; ++i) {
+                        if (i < nr) {
+                            const uint4 v =
+                                *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
+                            const mask_t m =
+                                *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
+                            const typename P::Sel sel = P::decode(m);
 #pragma unroll
-                        for (int b = 0; b < B; ++b)
-                            acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
+                            for (int b = 0; b < B; ++b)
+                                acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
+                        }
                     }
                 }
-            }
-            // Every lane has read the slot: refill it with this warp's task
-            // SW ahead (generic-proxy reads, then async-proxy writes of the
-            // same bytes: fence between them).
-            __syncwarp();
-            if (lane == 0 && issued < ntask && !failed) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                const int irt = warp + iss_n * W;
-                rows_issue<R, MB>(a, mt.values, mt.masks, sv, &my_full[slot], iss_kt, irt * R,
-                                  min(R, r_count - irt * R), r_begin, pol);
-                ++issued;
-                if (++iss_n == per_kt) {
-                    iss_n = 0;
-                    ++iss_kt;
+                // Every lane has read the slot: refill it with this warp's
+                // task SW ahead (generic-proxy reads, then async-proxy
+                // writes of the same bytes: fence between them).
+                __syncwarp();
+                if (lane == 0 && issued < ntask && !failed) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_next(sv, &my_full[slot]);
                 }
-            }
-            if (++slot == a.SW) {
-                slot = 0;
-                phase ^= 1u;
+                if (++slot == a.SW) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
             }
 
             warp_reduce_scatter<V>(acc, lane);
@@ -300,7 +358,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 // ---------------------------------------------------------------- host side
 
 struct RowsPlan {
-    int W, R, ktiles, tile_chunks, SW, grid;
+    int W, R, ktiles, tile_chunks, seg_chunks, nseg, nseg_last, SW, grid;
     int seg_v, seg_m, stage_bytes, xbuf_bytes, off_x, off_bar, off_carry;
     size_t smem;
 };
@@ -309,9 +367,15 @@ struct RowsPlan {
 // false if nothing fits in shared memory (the caller then takes another
 // kernel).  rows_plan_group does the same for `count` matrices with the same
 // K in one launch and writes each matrix's first CTA to cta_begin[0..count].
-bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, RowsPlan *out);
+// max_warps caps the warps per CTA.
+bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
+               RowsPlan *out);
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
-                     int max_smem, RowsPlan *out, int *cta_begin);
+                     int max_smem, int max_warps, RowsPlan *out, int *cta_begin);
+
+// Shared memory and registers one CTA may take so that two fit on an SM
+// (cached per device); false if the device cannot say.
+bool rows_pair_limits(int *smem_per_cta, int *regs_per_cta);
 
 template <int N, int M, int B, int R>
 cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const int *cta_begin,
@@ -325,6 +389,12 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     const int need = static_cast<int>(pl.smem);
     if (dev < 0 || dev >= 64 || need > smem_set[dev].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+        if (e != cudaSuccess) return e;
+        // Every instance asks for the same (largest) shared-memory carve-out,
+        // so CTAs of consecutive calls never wait for an SM to be
+        // reconfigured before they can share it.
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) {
             int cur = smem_set[dev].load(std::memory_order_relaxed);
@@ -343,12 +413,13 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
         m.x = static_cast<const __half *>(p.x);
         m.y = p.y;
         m.ldy = p.ldy;
-        m.cta_begin = cta_begin[i];
+        a.cta_begin[i] = cta_begin[i];
         const int ctas = cta_begin[i + 1] - cta_begin[i];
         m.row_base = static_cast<int>(p.rows / ctas);
         m.row_extra = static_cast<int>(p.rows % ctas);
     }
     a.nmat = g.count;
+    a.cta_begin[g.count] = cta_begin[g.count];
     a.err = p0.err;
     a.ldx = p0.ldx;
     a.vrow_bytes = p0.K / P::CK * 16;
@@ -356,7 +427,15 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     a.chunks = static_cast<int>(p0.K / P::CK);
     a.tile_chunks = pl.tile_chunks;
     a.ktiles = pl.ktiles;
+    a.seg_chunks = pl.seg_chunks;
+    a.nseg = pl.nseg;
+    a.nseg_last = pl.nseg_last;
     a.SW = pl.SW;
+    a.pre = std::min(bulk_tuning().rows_pre, pl.SW);
+    // L2 warm-up only where the CTA consumes its rows in address order (one K tile)
+    a.l2pre_rows = pl.ktiles == 1 ? static_cast<int>(bulk_tuning().rows_l2pre_bytes /
+                                                     (a.vrow_bytes + a.mrow_bytes))
+                                  : 0;
     a.seg_v = pl.seg_v;
     a.seg_m = pl.seg_m;
     a.stage_bytes = pl.stage_bytes;
@@ -365,7 +444,6 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     a.off_bar = pl.off_bar;
     a.off_carry = pl.off_carry;
     a.y_f32 = p0.y_f32 ? 1 : 0;
-    a.pf_bytes = bulk_tuning().l2_prefetch_bytes;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cta_begin[g.count]);
@@ -378,6 +456,32 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     cfg.attrs = attr;
     cfg.numAttrs = bulk_tuning().pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Registers per thread of one kernel instance (0 if unknown).
+template <int N, int M, int B, int R>
+int rows_instance_regs()
+{
+    static std::atomic<int> regs{-1};
+    int r = regs.load(std::memory_order_relaxed);
+    if (r < 0) {
+        cudaFuncAttributes fa;
+        r = cudaFuncGetAttributes(&fa, nm_spmv_rows_kernel<N, M, B, R>) == cudaSuccess
+                ? fa.numRegs : 0;
+        regs.store(r, std::memory_order_relaxed);
+    }
+    return r;
+}
+
+template <int N, int M, int B>
+int rows_regs(int R)
+{
+    switch (R) {
+    case 1: return rows_instance_regs<N, M, B, 1>();
+    case 2: return rows_instance_regs<N, M, B, 2>();
+    case 4: return rows_instance_regs<N, M, B, 4>();
+    default: return 0;
+    }
 }
 
 template <int N, int M, int B>
@@ -408,18 +512,38 @@ cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
     RowsPlan pl;
     int cta_begin[kRowsMaxGroup + 1];
     const int chunks = static_cast<int>(p0.K / P::CK);
-    if (g.count == 1) {
-        if (!rows_plan(p0.rows, chunks, P::CK, p0.batch, nsm, max_smem, &pl))
-            return cudaErrorNotSupported;
-        cta_begin[0] = 0;
-        cta_begin[1] = pl.grid;
-    } else {
-        int64_t rows[kRowsMaxGroup];
-        for (int i = 0; i < g.count; ++i) rows[i] = g.p[i].rows;
-        if (!rows_plan_group(rows, g.count, chunks, P::CK, p0.batch, nsm, max_smem, &pl,
-                             cta_begin))
-            return cudaErrorNotSupported;
+    int64_t rows[kRowsMaxGroup];
+    for (int i = 0; i < g.count; ++i) rows[i] = g.p[i].rows;
+    auto plan = [&](int smem_cap, int max_warps) {
+        if (g.count == 1) {
+            if (!rows_plan(p0.rows, chunks, P::CK, p0.batch, nsm, smem_cap, max_warps, &pl))
+                return false;
+            cta_begin[0] = 0;
+            cta_begin[1] = pl.grid;
+            return true;
+        }
+        return rows_plan_group(rows, g.count, chunks, P::CK, p0.batch, nsm, smem_cap, max_warps,
+                               &pl, cta_begin);
+    };
+    // Half an SM per CTA when the plan allows it (the warp cap follows from
+    // the chosen instance's registers, allocated 8 a thread at a time);
+    // otherwise the whole SM.
+    bool planned = false;
+    int pair_smem = 0, pair_regs = 0;
+    if (bulk_tuning().rows_pair && bulk_tuning().ctas_per_sm == 1 &&
+        rows_pair_limits(&pair_smem, &pair_regs)) {
+        int max_warps = kRowsMaxWarps;
+        for (int attempt = 0; attempt < 3 && !planned; ++attempt) {
+            if (!plan(std::min(pair_smem, max_smem), max_warps)) break;
+            const int regs = p0.batch == 1 ? rows_regs<N, M, 1>(pl.R) : rows_regs<N, M, 2>(pl.R);
+            if (regs <= 0) break;
+            const int fit = pair_regs / (32 * ((regs + 7) / 8 * 8));
+            if (pl.W <= fit) planned = true;
+            else if (fit < 4) break;
+            else max_warps = fit;
+        }
     }
+    if (!planned && !plan(max_smem, kRowsMaxWarps)) return cudaErrorNotSupported;
     return p0.batch == 1 ? launch_rows_b<N, M, 1>(g, pl, cta_begin, s)
                          : launch_rows_b<N, M, 2>(g, pl, cta_begin, s);
 }

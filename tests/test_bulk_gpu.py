@@ -249,8 +249,11 @@ print(json.dumps({"fails": fails, "errors": errs}))
 @pytest.mark.parametrize("tune", ["warps=2,cpl=1,rows=0", "warps=3,cpl=2,R=1,rows=0",
                                   "ring=4096,rows=0", "R=3,ring=20000,rows=0", "pdl=0",
                                   "ctas=2,warps=4", "stage=1024,rows=0", "rows_R=1",
-                                  "rows_R=4,rows_warps=3", "rows_seg=1024", "rows_ring=4096",
-                                  "rows_warps=1,rows_seg=2048", "ctas=2"])
+                                  "rows_R=4,rows_warps=3", "rows_xtile=1024", "rows_ring=4096",
+                                  "rows_warps=1,rows_xtile=2048,rows_task=512", "ctas=2",
+                                  "rows_pair=1", "rows_task=512", "rows_pre=1",
+                                  "rows_xtile=4096,rows_task=1000,rows_pre=1",
+                                  "rows_pair=1,rows_pre=2"])
 def test_bulk_forced_tunings(tune):
     cases = [(5, 4096, 2, 4, 1), (301, 8192, 2, 4, 2), (77, 14336, 4, 8, 1),
              (150, 5120, 1, 4, 1), (64, 3072, 2, 8, 3), (33, 1024, 4, 4, 8)]
