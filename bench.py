@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6400.0
 # step, from an ncu capture of that step (profiles/); None until captured for
 # the current kernel.
 TRAFFIC_PER_LAUNCH = {
-    # profiles/nm_spmv_rows_llama31_8b_block_2of4_launches.md (21 launches)
-    ("llama31_8b_block", "2:4", 1, "unfused"): 35.095e6,
+    # profiles/nm_spmv_rows_llama31_8b_block_2of4_launches.md (12 launches)
+    ("llama31_8b_block", "2:4", 1, "fused"): 61.441e6,
 }
 
 
@@ -116,6 +116,14 @@ class ClockSampler:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 9:
                 self.samples.append((time.time(), parts))
+
+    def wait_first(self, timeout: float = 3.0):
+        """Block until nvidia-smi has printed a sample (its start-up is done,
+        so it cannot stall the timed region), at most `timeout` seconds."""
+        t_end = time.time() + timeout
+        while self.proc is not None and not self.samples and time.time() < t_end:
+            time.sleep(0.01)
+        return self
 
     def stop(self):
         if self.proc is not None:
@@ -513,12 +521,13 @@ def run_ours(args, world, rank, local):
     streams = variants[args.launch]
     other = "unfused" if args.launch == "fused" else "fused"
 
-    sampler = ClockSampler(local).start() if rank == 0 else None
+    sampler = ClockSampler(local).start().wait_first() if rank == 0 else None
     dt, t_wall0, t_wall1 = time_steps(streams, copies, args.steps, args.warmup, world)
     dt = max_over_ranks(dt, world)
     launches = streams[0].launches * args.steps
     if sampler is not None:
         sampler.stop()
+        time.sleep(0.5)  # nvidia-smi's shutdown has been seen to stall the GPU briefly
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     # the other launch structure of the same step, same protocol
     odt, _, _ = time_steps(variants[other], copies, args.steps, args.warmup, world)
