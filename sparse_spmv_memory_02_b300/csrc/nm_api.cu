@@ -226,9 +226,9 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
     return NM_OK;
 }
 
-// One product on the best kernel that applies: the row-per-warp kernel
-// (batch <= 2), the chunk-column kernel, the direct-load kernel, the scalar
-// kernel.
+// One product on the best kernel that applies: the row kernel (any batch;
+// K a multiple of 128), the chunk-column kernel (when no row plan fits in
+// shared memory), the direct-load kernel, the scalar kernel.
 nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
@@ -382,8 +382,7 @@ nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
-    if (fusable && g.count > 1 && g.p[0].batch <= 2 &&
-        nm::bulk_path_applies(g.p[0].N, g.p[0].M, g.p[0].K))
+    if (fusable && g.count > 1 && nm::bulk_path_applies(g.p[0].N, g.p[0].M, g.p[0].K))
         e = nm::launch_rows(g, s);
     if (e == cudaSuccess) return NM_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "nm_spmv_group launch");

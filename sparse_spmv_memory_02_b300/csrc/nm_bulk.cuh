@@ -259,7 +259,7 @@ struct BulkTuning {
     int ring_bytes = 98304;  // shared memory for the ring
     int ctas_per_sm = 1;
     int pdl = 1;             // programmatic dependent launch
-    // row-per-warp kernel (batch 1 and 2)
+    // row kernel (batch 1 to 8)
     int rows_kernel = 1;           // 0: never take it
     int rows_warps = 0;            // warps per CTA (0: 16)
     int rows_R = 0;                // rows per task (0: chosen)

@@ -215,9 +215,14 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
     //    tile row longer than that is cut into even segments of a multiple
     //    of 32 chunks.  Smaller tasks are tried until everything fits with
     //    at least two slots per warp.
+    // Three or more vectors: two rows per task (R * B partial sums per lane
+    // stay <= 16), so each x unit read from shared memory serves two rows;
+    // the task size then bounds the two rows' segments.
+    const int R_many = t.rows_R ? std::min(t.rows_R, rows_rmax(B)) : 2;
     for (int target = t.rows_task_bytes; target >= 512; target /= 2) {
+        const int per_row = B >= 3 ? std::max(512, target / R_many) : target;
         const int64_t tile_bytes = static_cast<int64_t>(p.tile_chunks) * (16 + MB);
-        int64_t nseg = std::max<int64_t>(1, (tile_bytes + target - 1) / target);
+        int64_t nseg = std::max<int64_t>(1, (tile_bytes + per_row - 1) / per_row);
         int64_t seg = (p.tile_chunks + nseg - 1) / nseg;
         if (nseg > 1) seg = (seg + 31) / 32 * 32;
         if (seg >= p.tile_chunks) seg = p.tile_chunks;
@@ -228,13 +233,15 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
         p.seg_m = round_up(p.seg_chunks * MB, 16);
         const int segb = p.seg_v + p.seg_m;
 
-        // Rows per task: the largest of 1, 2, 4 with R * segb <= target
-        // (R * B partial sums per lane stay <= 8), whole tile rows only.
+        // One or two vectors: the largest of 1, 2, 4 rows with R * segb <=
+        // target (R * B partial sums per lane stay <= 8), whole tile rows
+        // only.
         int R = 1;
-        if (t.rows_R) R = p.nseg == 1 ? t.rows_R : 1;
+        if (B >= 3) R = R_many;
+        else if (t.rows_R) R = p.nseg == 1 ? t.rows_R : 1;
         else
             while (p.nseg == 1 && R < 4 && 2 * R * segb <= target && 2 * R * B <= 8) R *= 2;
-        if (R * B > 8) return false;
+        if (R > rows_rmax(B)) return false;
         p.R = R;
         p.stage_bytes = R * segb;
 
@@ -265,7 +272,7 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
 bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
                RowsPlan *out)
 {
-    if (rows <= 0 || chunks <= 0 || B < 1 || B > 2) return false;
+    if (rows <= 0 || chunks <= 0 || B < 1 || B > NM_MAX_BATCH) return false;
     const BulkTuning &t = bulk_tuning();
     if (!t.rows_kernel) return false;
     // One wave of CTAs; more only if the carried partial sums of a CTA's rows
@@ -281,7 +288,8 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, i
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
                      int max_smem, int max_warps, RowsPlan *out, int *cta_begin)
 {
-    if (count < 1 || count > kRowsMaxGroup || chunks <= 0 || B < 1 || B > 2) return false;
+    if (count < 1 || count > kRowsMaxGroup || chunks <= 0 || B < 1 || B > NM_MAX_BATCH)
+        return false;
     const BulkTuning &t = bulk_tuning();
     if (!t.rows_kernel) return false;
     int64_t total = 0;

@@ -1,6 +1,6 @@
-// N:M SpMV for one or two vectors: every warp owns whole rows and streams
+// N:M SpMV for one to eight vectors: every warp owns whole rows and streams
 // its own weights into shared memory with bulk (TMA) copies; x is held once
-// per CTA in shared memory.  The main kernel of libnm at batch 1.
+// per CTA in shared memory.  The main kernel of libnm.
 //
 // The operation is the N:M sparse matrix-vector product with bitmask
 // indexing and fixed-step traversal of "SparseDecoding: Decoding-Aware
@@ -33,6 +33,8 @@
 //
 // Per task, lane l walks the segment's chunk columns l, l+32, ...: it loads
 // the column's x units from shared memory once and uses them for all R rows
+// (from three vectors up, R = 2 and the vectors are taken a few at a time
+// so that their x words fit in registers)
 // (each a 16-byte value chunk plus its mask bits, decoded by byte permutes
 // in Pattern<N, M>), accumulating in fp32; after a row tile's last segment
 // the warp reduces its R*B sums with a reduce-scatter butterfly and one lane
@@ -105,6 +107,10 @@ struct RowsArgs {
 };
 
 constexpr int kRowsMaxWarps = 16;
+
+// Largest rows per task a batch size is built for (R * B partial sums per
+// lane: at most 8 for one or two vectors, 16 from three up).
+__host__ __device__ constexpr int rows_rmax(int B) { return B <= 2 ? 4 : 2; }
 
 // Copies task (K tile kt, segment sg, rows i0 .. i0+nr-1 of the CTA) into a
 // slot: the rows' value segments at st + i * seg_v, their mask segments at
@@ -291,31 +297,75 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                 const int cs = sg * a.seg_chunks;
                 const int ce = min(nc, cs + a.seg_chunks);
                 const uint8_t *xseg = xs + cs * 16;
+                if constexpr (B <= 2) {
 #pragma unroll 2
-                for (int c = lane; c < ce - cs; c += 32) {
-                    uint32_t xw[B][XR];
+                    for (int c = lane; c < ce - cs; c += 32) {
+                        uint32_t xw[B][XR];
 #pragma unroll
-                    for (int b = 0; b < B; ++b)
+                        for (int b = 0; b < B; ++b)
 #pragma unroll
-                        for (int u = 0; u < XV; ++u) {
-                            const uint4 t = *reinterpret_cast<const uint4 *>(
-                                xseg + ((b * XV + u) * a.tile_chunks + c) * 16);
-                            xw[b][4 * u + 0] = t.x;
-                            xw[b][4 * u + 1] = t.y;
-                            xw[b][4 * u + 2] = t.z;
-                            xw[b][4 * u + 3] = t.w;
+                            for (int u = 0; u < XV; ++u) {
+                                const uint4 t = *reinterpret_cast<const uint4 *>(
+                                    xseg + ((b * XV + u) * a.tile_chunks + c) * 16);
+                                xw[b][4 * u + 0] = t.x;
+                                xw[b][4 * u + 1] = t.y;
+                                xw[b][4 * u + 2] = t.z;
+                                xw[b][4 * u + 3] = t.w;
+                            }
+#pragma unroll
+                        for (int i = 0; i < R; ++i) {
+                            if (i < nr) {
+                                const uint4 v =
+                                    *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
+                                const mask_t m =
+                                    *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
+                                const typename P::Sel sel = P::decode(m);
+#pragma unroll
+                                for (int b = 0; b < B; ++b)
+                                    acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
+                            }
+                        }
+                    }
+                } else {
+                    // Three or more vectors: decode the R rows' chunks once,
+                    // then take the vectors BG at a time (x of BG vectors,
+                    // at most 32 words, in registers at once), each x unit
+                    // read once for R rows.
+                    constexpr int BG = B < 32 / XR ? B : (32 / XR > 0 ? 32 / XR : 1);
+                    for (int c = lane; c < ce - cs; c += 32) {
+                        uint4 v[R];
+                        typename P::Sel sel[R];
+#pragma unroll
+                        for (int i = 0; i < R; ++i) {
+                            if (i < nr) {
+                                v[i] = *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
+                                sel[i] = P::decode(
+                                    *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB));
+                            }
                         }
 #pragma unroll
-                    for (int i = 0; i < R; ++i) {
-                        if (i < nr) {
-                            const uint4 v =
-                                *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
-                            const mask_t m =
-                                *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
-                            const typename P::Sel sel = P::decode(m);
+                        for (int b0 = 0; b0 < B; b0 += BG) {
+                            uint32_t xw[BG][XR];
 #pragma unroll
-                            for (int b = 0; b < B; ++b)
-                                acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
+                            for (int bb = 0; bb < BG; ++bb)
+#pragma unroll
+                                for (int u = 0; u < XV; ++u) {
+                                    if (b0 + bb < B) {
+                                        const uint4 t = *reinterpret_cast<const uint4 *>(
+                                            xseg + (((b0 + bb) * XV + u) * a.tile_chunks + c) * 16);
+                                        xw[bb][4 * u + 0] = t.x;
+                                        xw[bb][4 * u + 1] = t.y;
+                                        xw[bb][4 * u + 2] = t.z;
+                                        xw[bb][4 * u + 3] = t.w;
+                                    }
+                                }
+#pragma unroll
+                            for (int i = 0; i < R; ++i)
+#pragma unroll
+                                for (int bb = 0; bb < BG; ++bb)
+                                    if (i < nr && b0 + bb < B)
+                                        acc[i * B + b0 + bb] =
+                                            P::dot(v[i], sel[i], xw[bb], acc[i * B + b0 + bb]);
                         }
                     }
                 }
@@ -479,7 +529,25 @@ int rows_regs(int R)
     switch (R) {
     case 1: return rows_instance_regs<N, M, B, 1>();
     case 2: return rows_instance_regs<N, M, B, 2>();
-    case 4: return rows_instance_regs<N, M, B, 4>();
+    case 4:
+        if constexpr (rows_rmax(B) >= 4) return rows_instance_regs<N, M, B, 4>();
+        return 0;
+    default: return 0;
+    }
+}
+
+template <int N, int M>
+int rows_regs_any(int B, int R)
+{
+    switch (B) {
+    case 1: return rows_regs<N, M, 1>(R);
+    case 2: return rows_regs<N, M, 2>(R);
+    case 3: return rows_regs<N, M, 3>(R);
+    case 4: return rows_regs<N, M, 4>(R);
+    case 5: return rows_regs<N, M, 5>(R);
+    case 6: return rows_regs<N, M, 6>(R);
+    case 7: return rows_regs<N, M, 7>(R);
+    case 8: return rows_regs<N, M, 8>(R);
     default: return 0;
     }
 }
@@ -491,12 +559,14 @@ cudaError_t launch_rows_b(const SpmvGroup &g, const RowsPlan &pl, const int *cta
     switch (pl.R) {
     case 1: return launch_rows_instance<N, M, B, 1>(g, pl, cta_begin, s);
     case 2: return launch_rows_instance<N, M, B, 2>(g, pl, cta_begin, s);
-    case 4: return launch_rows_instance<N, M, B, 4>(g, pl, cta_begin, s);
+    case 4:
+        if constexpr (rows_rmax(B) >= 4) return launch_rows_instance<N, M, B, 4>(g, pl, cta_begin, s);
+        return cudaErrorNotSupported;
     default: return cudaErrorNotSupported;
     }
 }
 
-// Batch 1 and 2 only; cudaErrorNotSupported (nothing launched) otherwise or
+// Batch 1 to 8; cudaErrorNotSupported (nothing launched) otherwise or
 // when no plan fits.  All problems of the group share N, M, K, batch, ldx
 // and the y type.
 template <int N, int M>
@@ -504,7 +574,8 @@ cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
 {
     using P = Pattern<N, M>;
     const SpmvProblem &p0 = g.p[0];
-    if (p0.batch > 2 || g.count < 1 || g.count > kRowsMaxGroup) return cudaErrorNotSupported;
+    if (p0.batch < 1 || p0.batch > NM_MAX_BATCH || g.count < 1 || g.count > kRowsMaxGroup)
+        return cudaErrorNotSupported;
     const int nsm = sm_count();
     if (nsm <= 0) return cudaErrorInvalidDevice;
     const int max_smem = max_dynamic_smem();
@@ -535,7 +606,7 @@ cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
         int max_warps = kRowsMaxWarps;
         for (int attempt = 0; attempt < 3 && !planned; ++attempt) {
             if (!plan(std::min(pair_smem, max_smem), max_warps)) break;
-            const int regs = p0.batch == 1 ? rows_regs<N, M, 1>(pl.R) : rows_regs<N, M, 2>(pl.R);
+            const int regs = rows_regs_any<N, M>(p0.batch, pl.R);
             if (regs <= 0) break;
             const int fit = pair_regs / (32 * ((regs + 7) / 8 * 8));
             if (pl.W <= fit) planned = true;
@@ -544,8 +615,17 @@ cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
         }
     }
     if (!planned && !plan(max_smem, kRowsMaxWarps)) return cudaErrorNotSupported;
-    return p0.batch == 1 ? launch_rows_b<N, M, 1>(g, pl, cta_begin, s)
-                         : launch_rows_b<N, M, 2>(g, pl, cta_begin, s);
+    switch (p0.batch) {
+    case 1: return launch_rows_b<N, M, 1>(g, pl, cta_begin, s);
+    case 2: return launch_rows_b<N, M, 2>(g, pl, cta_begin, s);
+    case 3: return launch_rows_b<N, M, 3>(g, pl, cta_begin, s);
+    case 4: return launch_rows_b<N, M, 4>(g, pl, cta_begin, s);
+    case 5: return launch_rows_b<N, M, 5>(g, pl, cta_begin, s);
+    case 6: return launch_rows_b<N, M, 6>(g, pl, cta_begin, s);
+    case 7: return launch_rows_b<N, M, 7>(g, pl, cta_begin, s);
+    case 8: return launch_rows_b<N, M, 8>(g, pl, cta_begin, s);
+    default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace nm
