@@ -293,7 +293,12 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                 }
                 uint8_t *sv = my_ring + static_cast<size_t>(slot) * a.stage_bytes;
                 const uint8_t *sm = sv + R * a.seg_v;
-                // columns [cs, ce) of the K tile; the slot holds them from 0
+                // columns [cs, ce) of the K tile; the slot holds them from 0.
+                // All R rows are computed even when the task has nr < R (the
+                // CTA's last row tile): the rows past nr read stale slot
+                // bytes -- the mask only feeds byte permutes, never an
+                // address -- and their sums are never stored.  This keeps
+                // the loop free of per-row branches.
                 const int cs = sg * a.seg_chunks;
                 const int ce = min(nc, cs + a.seg_chunks);
                 const uint8_t *xseg = xs + cs * 16;
@@ -314,16 +319,14 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                             }
 #pragma unroll
                         for (int i = 0; i < R; ++i) {
-                            if (i < nr) {
-                                const uint4 v =
-                                    *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
-                                const mask_t m =
-                                    *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
-                                const typename P::Sel sel = P::decode(m);
+                            const uint4 v =
+                                *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
+                            const mask_t m =
+                                *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
+                            const typename P::Sel sel = P::decode(m);
 #pragma unroll
-                                for (int b = 0; b < B; ++b)
-                                    acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
-                            }
+                            for (int b = 0; b < B; ++b)
+                                acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
                         }
                     }
                 } else {
@@ -337,11 +340,9 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                         typename P::Sel sel[R];
 #pragma unroll
                         for (int i = 0; i < R; ++i) {
-                            if (i < nr) {
-                                v[i] = *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
-                                sel[i] = P::decode(
-                                    *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB));
-                            }
+                            v[i] = *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
+                            sel[i] = P::decode(
+                                *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB));
                         }
 #pragma unroll
                         for (int b0 = 0; b0 < B; b0 += BG) {
@@ -363,7 +364,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                             for (int i = 0; i < R; ++i)
 #pragma unroll
                                 for (int bb = 0; bb < BG; ++bb)
-                                    if (i < nr && b0 + bb < B)
+                                    if (b0 + bb < B)
                                         acc[i * B + b0 + bb] =
                                             P::dot(v[i], sel[i], xw[bb], acc[i * B + b0 + bb]);
                         }
