@@ -217,7 +217,12 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
     //    at least two slots per warp.
     // Three or more vectors: two rows per task (R * B partial sums per lane
     // stay <= 16), so each x unit read from shared memory serves two rows;
-    // the task size then bounds the two rows' segments.
+    // the task size then bounds the two rows' segments together.  Patterns
+    // whose chunk spans 32 or more positions (x read per chunk is then at
+    // least four times the value bytes) also take two rows a task when a
+    // whole row fits the task size (measured: two-row tasks of short
+    // segments lose more to copy count than they save on x reads).
+    const bool two_rows = B >= 3;
     const int R_many = t.rows_R ? std::min(t.rows_R, rows_rmax(B)) : 2;
     for (int target = t.rows_task_bytes; target >= 512; target /= 2) {
         const int per_row = B >= 3 ? std::max(512, target / R_many) : target;
@@ -237,8 +242,9 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
         // target (R * B partial sums per lane stay <= 8), whole tile rows
         // only.
         int R = 1;
-        if (B >= 3) R = R_many;
+        if (two_rows) R = R_many;
         else if (t.rows_R) R = p.nseg == 1 ? t.rows_R : 1;
+        else if (CK >= 32 && p.nseg == 1) R = 2;  // whole rows: two copies a task
         else
             while (p.nseg == 1 && R < 4 && 2 * R * segb <= target && 2 * R * B <= 8) R *= 2;
         if (R > rows_rmax(B)) return false;
