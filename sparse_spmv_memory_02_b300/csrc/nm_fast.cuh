@@ -117,8 +117,11 @@ template <> struct Pattern<1, 4> {
 struct Pair8 { uint32_t s, pick; };
 __device__ __forceinline__ Pair8 pair8(uint32_t pa, uint32_t pb)
 {
-    return Pair8{sel_pair(pa & 3u, pb & 3u),
-                 ((pa & 4u) ? 0x54u : 0x10u) | ((pb & 4u) ? 0x7600u : 0x3200u)};
+    // Both selectors at once from q = pa | pb << 8: the within-half lane of
+    // each (bits 0-1 of each byte) scales the sel_pair step 0x22, the half
+    // (bit 2) scales the step 0x44 that moves a pick from lo's bytes to hi's.
+    const uint32_t q = pa | (pb << 8);
+    return Pair8{0x1010u + 0x22u * (q & 0x0303u), 0x3210u + 0x44u * ((q >> 2) & 0x0101u)};
 }
 __device__ __forceinline__ uint32_t gather8(const uint32_t *xg, const Pair8 &p)
 {
