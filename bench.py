@@ -60,9 +60,11 @@ def parse_args(argv=None):
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--copies", type=int, default=3, help="rotating packed copies (L2 defeat)")
     p.add_argument("--profile-steps", type=int, default=50, help="calls per layer in the per-layer pass")
-    p.add_argument("--launch", choices=["fused", "unfused"], default="fused",
+    p.add_argument("--launch", choices=["fused", "unfused", "fused_silu"], default="fused",
                    help="fused: layers reading the same input (q/k/v, gate/up) share one "
-                        "nm_spmv_group launch; unfused: one nm_spmv launch per layer")
+                        "nm_spmv_group launch; unfused: one nm_spmv launch per layer; "
+                        "fused_silu: as fused, with gate/up one nm_spmv_gate_up_silu launch "
+                        "writing silu(gate x) * (up x)")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -236,17 +238,31 @@ def build_workload(wl, N, M, batch, copies, device="cuda", keep_dense=False):
     return layers
 
 
-def step_bytes(layers, batch):
+def silu_pairs(layers):
+    """(gate, up) index pairs of consecutive gate and up layers (one per
+    decoder block)."""
+    return [(i, i + 1) for i in range(len(layers) - 1)
+            if layers[i]["name"] == "gate" and layers[i + 1]["name"] == "up"]
+
+
+def step_bytes(layers, batch, silu=False):
+    """Algorithmic bytes per layer call; with the gate/up SiLU epilogue the
+    up layer reads no x of its own and writes no y (the pair writes one h)."""
     from sparse_spmv_memory_02_b300.stream import algorithmic_bytes
-    return [algorithmic_bytes(L["mats"][0], batch, 2) for L in layers]
+    out = [algorithmic_bytes(L["mats"][0], batch, 2) for L in layers]
+    if silu:
+        for _, ui in silu_pairs(layers):
+            out[ui] -= batch * layers[ui]["K"] * 2 + batch * layers[ui]["rows"] * 2
+    return out
 
 
-def capture_step_graphs(layers, copies, fused):
+def capture_step_graphs(layers, copies, fused, silu=False):
     from sparse_spmv_memory_02_b300.stream import LayerStream
     streams = []
+    pairs = silu_pairs(layers) if silu else ()
     for c in range(copies):
         s = LayerStream([L["mats"][c] for L in layers], [L["x"] for L in layers],
-                        [L["y"] for L in layers], fuse_shared_input=fused)
+                        [L["y"] for L in layers], fuse_shared_input=fused, silu_pairs=pairs)
         s.capture()
         streams.append(s)
     return streams
@@ -316,6 +332,65 @@ def layer_pass(layers, batch, reps, l2_bytes):
         out.append(statistics.median(times))
         del g, extra, mats
         torch.cuda.empty_cache()
+    return out
+
+
+def _graph_time(run, n):
+    """Median seconds per call of `run` (n calls) replayed from a CUDA graph."""
+    run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            run()
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(5):
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3 / n)
+    del g
+    return statistics.median(times)
+
+
+def pair_pass(gate, up, batch, reps, l2_bytes):
+    """The gate/up pair alone, as one nm_spmv_group launch (two outputs) and
+    as one nm_spmv_gate_up_silu launch (silu(gate x) * (up x)), each a CUDA
+    graph of calls rotating over > 3x L2 of packed copies.  Returns
+    {variant: (seconds per call, algorithmic bytes per call)}."""
+    from sparse_spmv_memory_02_b300 import nm
+    from sparse_spmv_memory_02_b300.stream import algorithmic_bytes
+    G, U = gate["mats"][0], up["mats"][0]
+    ncopy = max(3, -(-3 * l2_bytes // (G.nbytes + U.nbytes)))
+    gs = [G] + [nm.PackedMatrix(G.values.clone(), G.masks.clone(), G.rows, G.K, G.N, G.M)
+                for _ in range(ncopy - 1)]
+    us = [U] + [nm.PackedMatrix(U.values.clone(), U.masks.clone(), U.rows, U.K, U.N, U.M)
+                for _ in range(ncopy - 1)]
+    n = max(reps, ncopy)
+    x, yg, yu = gate["x"], gate["y"], up["y"]
+
+    def run_group():
+        for i in range(n):
+            nm.nm_spmv_group([gs[i % ncopy], us[i % ncopy]], [x, x], [yg, yu])
+
+    def run_silu():
+        for i in range(n):
+            nm.nm_spmv_gate_up_silu(gs[i % ncopy], us[i % ncopy], x, yg)
+
+    b_group = algorithmic_bytes(G, batch, 2) + algorithmic_bytes(U, batch, 2)
+    b_silu = b_group - batch * U.K * 2 - batch * U.rows * 2
+    out = {"group": (_graph_time(run_group, n), b_group),
+           "silu": (_graph_time(run_silu, n), b_silu)}
+    del gs, us
+    torch.cuda.empty_cache()
     return out
 
 
@@ -457,10 +532,14 @@ def config_block(args, wl, N, M, copies, layers_desc):
     return {"workload": wl.key, "title": wl.title, "pattern": "%d:%d" % (N, M),
             "batch": args.batch, "layers": layers_desc,
             "l2": "rotating %d packed copies of the step's weights (> 3x the 126 MB L2)" % copies,
-            "launch": "one CUDA graph per step: %s" % (
-                "q/k/v and gate/up each one nm_spmv_group launch (they read the same input), "
-                "o and down one nm_spmv launch each" if getattr(args, "launch", "") == "fused"
-                else "one nm_spmv launch per layer"),
+            "launch": "one CUDA graph per step: %s" % {
+                "fused": "q/k/v and gate/up each one nm_spmv_group launch (they read the same "
+                         "input), o and down one nm_spmv launch each",
+                "fused_silu": "q/k/v one nm_spmv_group launch, o and down one nm_spmv launch "
+                              "each, gate/up one nm_spmv_gate_up_silu launch writing "
+                              "silu(gate x) * (up x)",
+                "unfused": "one nm_spmv launch per layer"}.get(getattr(args, "launch", ""),
+                                                               "one nm_spmv launch per layer"),
             "weights": "synthetic N(0,0.02), top-N |w| per group of M along K",
             "activations": ("synthetic N(0,1), 1% outlier channels x20; q/k/v share one input "
                             "vector, gate/up another" if wl.outliers else "synthetic N(0,1)")}
@@ -515,11 +594,17 @@ def run_ours(args, world, rank, local):
         copies = 1  # one step already streams more than 3x L2
     layers = build_workload(wl, N, M, args.batch, copies, keep_dense=not args.no_dense)
     bytes_per_call = step_bytes(layers, args.batch)
-    step_b = sum(bytes_per_call)
     variants = {"fused": capture_step_graphs(layers, copies, fused=True),
                 "unfused": capture_step_graphs(layers, copies, fused=False)}
+    variant_bytes = {"fused": sum(bytes_per_call), "unfused": sum(bytes_per_call)}
+    if silu_pairs(layers):
+        variants["fused_silu"] = capture_step_graphs(layers, copies, fused=True, silu=True)
+        variant_bytes["fused_silu"] = sum(step_bytes(layers, args.batch, silu=True))
+    if args.launch not in variants:
+        raise SystemExit("--launch %s: this workload has no gate/up layers" % args.launch)
     streams = variants[args.launch]
-    other = "unfused" if args.launch == "fused" else "fused"
+    step_b = variant_bytes[args.launch]
+    others = [k for k in variants if k != args.launch]
 
     sampler = ClockSampler(local).start().wait_first() if rank == 0 else None
     dt, t_wall0, t_wall1 = time_steps(streams, copies, args.steps, args.warmup, world)
@@ -529,14 +614,29 @@ def run_ours(args, world, rank, local):
         sampler.stop()
         time.sleep(0.5)  # nvidia-smi's shutdown has been seen to stall the GPU briefly
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
-    # the other launch structure of the same step, same protocol
-    odt, _, _ = time_steps(variants[other], copies, args.steps, args.warmup, world)
-    odt = max_over_ranks(odt, world)
+    # the other launch structures of the same step, same protocol
+    other_launch = {}
+    for k in others:
+        odt, _, _ = time_steps(variants[k], copies, args.steps, args.warmup, world)
+        odt = max_over_ranks(odt, world)
+        other_launch[k] = {"launches_per_step": variants[k][0].launches,
+                           "us_per_step": odt / args.steps * 1e6,
+                           "value": variant_bytes[k] * args.steps / odt / 1e9}
 
     # each layer alone, L2-cold, for the per-layer figures
     l2_bytes = l2
     first_block = layers[:len(wl.layers)]
     layer_t = layer_pass(first_block, args.batch, args.profile_steps, l2_bytes)
+    gate_up = None
+    fp = silu_pairs(first_block)
+    if fp:
+        gi, ui = fp[0]
+        pp = pair_pass(first_block[gi], first_block[ui], args.batch, args.profile_steps, l2_bytes)
+        gate_up = {k: {"us": t * 1e6, "bytes": b, "gbs": b / t / 1e9, "frac_of_peak": None}
+                   for k, (t, b) in pp.items()}
+        gate_up["note"] = ("the block's gate and up projections alone: one nm_spmv_group "
+                           "launch writing both outputs, or one nm_spmv_gate_up_silu launch "
+                           "writing silu(gate x) * (up x)")
 
     dense = None
     if not args.no_dense:
@@ -577,6 +677,9 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
+    if gate_up:
+        for k in ("group", "silu"):
+            gate_up[k]["frac_of_peak"] = gate_up[k]["gbs"] / peak
     value = world * step_b * args.steps / dt / 1e9
     achieved = step_b * args.steps / dt / 1e9  # this rank's step: all launches are the SpMV kernel
     per_layer = {}
@@ -594,14 +697,13 @@ def run_ours(args, world, rank, local):
         "us_per_call_note": "each layer alone, a CUDA graph of calls rotating over > 3x L2 of "
                             "packed copies",
         "per_layer": per_layer,
+        "gate_up": gate_up,
         "step_algorithmic_bytes": step_b,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,
-        "launch": {"structure": args.launch, "launches_per_step": streams[0].launches,
-                   "groups": [[layers[i]["name"] for i in g] for g in streams[0].groups],
-                   other: {"launches_per_step": variants[other][0].launches,
-                           "us_per_step": odt / args.steps * 1e6,
-                           "value": step_b * args.steps / odt / 1e9}},
+        "launch": dict({"structure": args.launch, "launches_per_step": streams[0].launches,
+                        "groups": [[layers[i]["name"] for i in g] for g in streams[0].groups]},
+                       **other_launch),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": TRAFFIC_PER_LAUNCH.get(
                          (wl.key, "%d:%d" % (N, M), args.batch, args.launch)),

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 110 /* 1.1.0 */
+#define NM_VERSION 120 /* 1.2.0 */
 #define NM_MAX_BATCH 8
 #define NM_MAX_GROUP 8
 
@@ -202,6 +202,29 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
                         void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
                         nm_stream_t stream);
+
+/*
+ * The gated MLP input of a decoder layer in one pass over both weight
+ * matrices: h[b][i] = silu(gate_i . x_b) * (up_i . x_b), silu(g) =
+ * g / (1 + exp(-g)), for i < rows and b < batch.  The decoder layers of the
+ * model families the pages measure (Llama-3.1, Llama-3.3, Qwen3:
+ * "SparseDecoding Makes LLM Pruning Aware of Generation", Introduction)
+ * feed their down projection with this product of the gate and up
+ * projections, which both read the MLP input; computing it in the SpMV's
+ * epilogue saves the two intermediate vectors and a kernel boundary.
+ *   gate, up  packed matrices with the same rows, K, N and M.
+ *   x         fp16 [batch][ldx], device (as nm_spmv_batched).
+ *   h         h_type [batch][ldh], device; ldh >= rows.
+ * Both dot products are carried in fp32 as by nm_spmv; silu and the product
+ * are evaluated in fp32 and h is rounded once.  Errors as nm_spmv_batched;
+ * in addition NM_ERR_INVALID_ARG if gate and up differ in shape, and
+ * NM_ERR_UNSUPPORTED unless K is a multiple of 128 and 8 % N == 0 (the
+ * shapes the streaming kernel takes).  Asynchronous, allocates nothing, may
+ * be captured in a CUDA graph; overlaps the preceding kernel as nm_spmv.
+ */
+nm_status nm_spmv_gate_up_silu(const nm_matrix *gate, const nm_matrix *up, const void *x,
+                               int64_t ldx, void *h, int64_t ldh, int batch, nm_dtype h_type,
+                               nm_stream_t stream);
 
 /*
  * Read the device error word of the calling thread's current device into

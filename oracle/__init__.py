@@ -182,6 +182,37 @@ def topn_mask(W, N: int, M: int) -> np.ndarray:
     return mask
 
 
+def silu(g):
+    """silu(g) = g / (1 + exp(-g)) in fp64, elementwise (exp overflow for
+    g < -709 gives -0.0, the limit)."""
+    g = np.asarray(g, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+# Largest slope of silu: silu'(g) = s(g) (1 + g (1 - s(g))), s the logistic
+# function; its maximum, about 1.0998 near g = 2.3994, rounded up.
+SILU_LIPSCHITZ = 1.1
+
+
+def gate_up_silu(Wg, mg, Wu, mu, x, rel: float = 1e-3, abs_: float = 1e-6):
+    """Reference h[b][i] = silu(g) * u with g = (Wg (.) mg) x_b and
+    u = (Wu (.) mu) x_b computed by spmv_dense in fp64, and a per-element
+    bound on |h - h_ref| for a kernel whose g and u each meet the SpMV
+    tolerance |d| <= rel * s + abs_:
+        L e_g (|u| + e_u) + |silu(g)| e_u + 2**-10 |h| + 1e-6
+    (silu is L-Lipschitz; the last terms cover evaluating silu and the
+    product in fp32 and rounding h to fp16).  Returns (h_ref, bound)."""
+    g, sg = spmv_dense(Wg, mg, x)
+    u, su = spmv_dense(Wu, mu, x)
+    eg = rel * sg + abs_
+    eu = rel * su + abs_
+    h = silu(g) * u
+    bound = (SILU_LIPSCHITZ * eg * (np.abs(u) + eu) + np.abs(silu(g)) * eu
+             + 2.0 ** -10 * np.abs(h) + 1e-6)
+    return h, bound
+
+
 def within_tolerance(y_gpu, y_ref, s_ref, rel: float = 1e-3, abs_: float = 1e-6):
     """Per-element acceptance rule |y - y_ref| <= rel * s + abs."""
     y_gpu = np.asarray(y_gpu, dtype=np.float64)

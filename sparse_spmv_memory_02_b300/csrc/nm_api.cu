@@ -349,6 +349,47 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx, void *
     return run_product(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+nm_status nm_spmv_gate_up_silu(const nm_matrix *gate, const nm_matrix *up, const void *x,
+                               int64_t ldx, void *h, int64_t ldh, int batch, nm_dtype h_type,
+                               nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    if (!gate || !up) return fail(NM_ERR_INVALID_ARG, "gate and up must be non-NULL");
+    if (gate->rows != up->rows || gate->K != up->K || gate->N != up->N || gate->M != up->M)
+        return fail(NM_ERR_INVALID_ARG, "gate and up must have the same rows, K, N and M");
+    nm_status st = check_matrix(gate);
+    if (st != NM_OK) return st;
+    if (gate->rows > 0 && gate->K > 0 && !nm::bulk_path_applies(gate->N, gate->M, gate->K))
+        return fail(NM_ERR_UNSUPPORTED,
+                    "nm_spmv_gate_up_silu: K must be a multiple of 128 and N:M one of 1:4, "
+                    "2:4, 4:4, 1:8, 2:8, 4:8, 8:8 (K=%lld, %d:%d)",
+                    (long long)gate->K, gate->N, gate->M);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    nm::SpmvGroup g;
+    g.count = 2;
+    g.pair = true;
+    bool empty_gate = false, empty_up = false;
+    st = prepare_product(gate, x, ldx, h, ldh, batch, h_type, &g.p[0], &empty_gate, s);
+    if (st != NM_OK) {
+        char msg[512];
+        snprintf(msg, sizeof(msg), "gate: %s", g_last_error);
+        return fail(st, "%s", msg);
+    }
+    st = prepare_product(up, x, ldx, h, ldh, batch, h_type, &g.p[1], &empty_up, s);
+    if (st != NM_OK) {
+        char msg[512];
+        snprintf(msg, sizeof(msg), "up: %s", g_last_error);
+        return fail(st, "%s", msg);
+    }
+    if (empty_gate) return NM_OK;  // rows == 0, or K == 0 and h zeroed (silu(0) * 0 = 0)
+    const cudaError_t e = nm::launch_rows(g, s);
+    if (e == cudaErrorNotSupported)
+        return fail(NM_ERR_UNSUPPORTED, "nm_spmv_gate_up_silu: no kernel plan fits K=%lld",
+                    (long long)gate->K);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_spmv_gate_up_silu launch");
+    return NM_OK;
+}
+
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
                         void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
                         nm_stream_t stream)

@@ -184,7 +184,7 @@ namespace {
 // The row kernel's plan for a K (in chunks), batch and a grid whose busiest
 // CTA has rows_per_cta rows.
 bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, int max_smem,
-                    int max_warps, RowsPlan *out)
+                    int max_warps, RowsPlan *out, bool pair = false)
 {
     const BulkTuning &t = bulk_tuning();
     const int MB = CK / 8;  // mask bytes per chunk
@@ -207,7 +207,7 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
     const int last_chunks = chunks - (p.ktiles - 1) * p.tile_chunks;
     p.xbuf_bytes = B * (CK / 8) * p.tile_chunks * 16;
     const int nxb = p.ktiles > 1 ? 2 : 1;
-    const int64_t carry64 = p.ktiles > 1 ? rows_per_cta * B * 4 : 0;
+    const int64_t carry64 = p.ktiles > 1 ? rows_per_cta * B * 4 * (pair ? 2 : 1) : 0;
     if (carry64 > 64 * 1024) return false;
     const int carry = static_cast<int>(carry64);
 
@@ -222,10 +222,11 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
     // least four times the value bytes) also take two rows a task when a
     // whole row fits the task size (measured: two-row tasks of short
     // segments lose more to copy count than they save on x reads).
-    const bool two_rows = B >= 3;
+    // (A gate/up pair always takes two rows a task: one of each matrix.)
+    const bool two_rows = B >= 3 || pair;
     const int R_many = t.rows_R ? std::min(t.rows_R, rows_rmax(B)) : 2;
     for (int target = t.rows_task_bytes; target >= 512; target /= 2) {
-        const int per_row = B >= 3 ? std::max(512, target / R_many) : target;
+        const int per_row = two_rows ? std::max(512, target / R_many) : target;
         const int64_t tile_bytes = static_cast<int64_t>(p.tile_chunks) * (16 + MB);
         int64_t nseg = std::max<int64_t>(1, (tile_bytes + per_row - 1) / per_row);
         int64_t seg = (p.tile_chunks + nseg - 1) / nseg;
@@ -242,7 +243,8 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
         // target (R * B partial sums per lane stay <= 8), whole tile rows
         // only.
         int R = 1;
-        if (two_rows) R = R_many;
+        if (pair) R = 2;
+        else if (two_rows) R = R_many;
         else if (t.rows_R) R = p.nseg == 1 ? t.rows_R : 1;
         else if (CK >= 32 && p.nseg == 1) R = 2;  // whole rows: two copies a task
         else
@@ -276,7 +278,7 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
 }  // namespace
 
 bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
-               RowsPlan *out)
+               RowsPlan *out, bool pair)
 {
     if (rows <= 0 || chunks <= 0 || B < 1 || B > NM_MAX_BATCH) return false;
     const BulkTuning &t = bulk_tuning();
@@ -288,7 +290,7 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, i
     grid = std::max<int64_t>(grid, (rows + max_rows - 1) / max_rows);
     if (grid > 0x7fffffff) return false;
     return rows_plan_impl((rows + grid - 1) / grid, static_cast<int>(grid), chunks, CK, B,
-                          max_smem, max_warps, out);
+                          max_smem, max_warps, out, pair);
 }
 
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,

@@ -31,6 +31,9 @@ struct SpmvProblem {
 struct SpmvGroup {
     int count;
     SpmvProblem p[NM_MAX_GROUP];
+    // Gate/up pair (count == 2, same shape): one output per row,
+    // p[0].y = silu(p[0] x) * (p[1] x); p[1].y is unused.
+    bool pair = false;
 };
 
 // Vectorised kernel: 8 % N == 0 and K a multiple of the k-span of one

@@ -80,6 +80,8 @@ struct RowsMat {
     void *y;                // [B][ldy]
     int64_t ldy;
     int row_base, row_extra;  // its CTA c owns row_base rows (+1 if c < row_extra)
+    const uint8_t *values2;   // gate/up pair: the up matrix (same shape as this one)
+    const uint8_t *masks2;
 };
 
 // The scalars every CTA reads first come first (kernel parameters are read
@@ -99,6 +101,7 @@ struct RowsArgs {
     int xbuf_bytes;         // one x tile buffer: B * XV * tile_chunks * 16
     int off_x, off_bar, off_carry;
     int y_f32;
+    int pair;               // 1: gate/up pair, y = silu(gate x) * (up x) (R == 2)
     int l2pre_rows;         // rows per CTA warmed in L2 before the dependence wait
     int cta_begin[kRowsMaxGroup + 1];  // first CTA of each matrix; [nmat] = grid
     int64_t ldx, vrow_bytes, mrow_bytes;
@@ -126,8 +129,21 @@ __device__ __forceinline__ void rows_issue(const RowsArgs &a, const uint8_t *val
     const int nc = min(a.seg_chunks, min(a.tile_chunks, a.chunks - t0) - sg * a.seg_chunks);
     const uint32_t vb = static_cast<uint32_t>(nc) * 16u;
     const uint32_t mb = static_cast<uint32_t>(nc) * MB;
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * (vb + mb));
     const int64_t row0 = r_begin + i0;
+    if (R == 2 && a.pair) {
+        // gate/up pair: output row row0 is slot row 0 of the gate matrix
+        // and slot row 1 of the up matrix
+        const RowsMat &m = a.mat[0];
+        mbar_arrive_expect_tx(bar, 2u * (vb + mb));
+        bulk_g2s(st, values + row0 * a.vrow_bytes + c0 * 16LL, vb, bar, pol);
+        bulk_g2s(st + a.seg_v, m.values2 + row0 * a.vrow_bytes + c0 * 16LL, vb, bar, pol);
+        bulk_g2s(st + R * a.seg_v, masks + row0 * a.mrow_bytes + static_cast<int64_t>(c0) * MB,
+                 mb, bar, pol);
+        bulk_g2s(st + R * a.seg_v + a.seg_m,
+                 m.masks2 + row0 * a.mrow_bytes + static_cast<int64_t>(c0) * MB, mb, bar, pol);
+        return;
+    }
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nr) * (vb + mb));
     if (R == 1 || a.seg_chunks == a.chunks) {
         // one row, or whole rows (then seg_v == vrow_bytes and seg_m ==
         // mrow_bytes): one contiguous range of each array, in the slot's layout
@@ -176,7 +192,8 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     const int cta = static_cast<int>(blockIdx.x) - a.cta_begin[mi];
     const int r_begin = cta * mt.row_base + min(cta, mt.row_extra);
     const int r_count = mt.row_base + (cta < mt.row_extra ? 1 : 0);
-    const int nrt = (r_count + R - 1) / R;                         // row tiles of the CTA
+    const int RT = a.pair ? 1 : R;  // output rows per row tile (a pair tile is one row of each)
+    const int nrt = (r_count + RT - 1) / RT;                       // row tiles of the CTA
     const int per_kt = nrt > warp ? (nrt - warp + W - 1) / W : 0;  // this warp's tiles per K tile
     const int ntask = per_kt * ((a.ktiles - 1) * a.nseg + a.nseg_last);
     uint8_t *my_ring = ring + static_cast<size_t>(warp) * a.SW * a.stage_bytes;
@@ -197,8 +214,8 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     int iss_kt = 0, iss_n = 0, iss_s = 0;
     auto issue_next = [&](uint8_t *st, uint64_t *bar) {
         const int rt = warp + iss_n * W;
-        rows_issue<R, MB>(a, mt.values, mt.masks, st, bar, iss_kt, iss_s, rt * R,
-                          min(R, r_count - rt * R), r_begin, pol);
+        rows_issue<R, MB>(a, mt.values, mt.masks, st, bar, iss_kt, iss_s, rt * RT,
+                          min(RT, r_count - rt * RT), r_begin, pol);
         ++issued;
         if (++iss_s == (iss_kt == a.ktiles - 1 ? a.nseg_last : a.nseg)) {
             iss_s = 0;
@@ -281,8 +298,8 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 
         for (int n = 0; n < per_kt; ++n) {
             const int rt = warp + n * W;
-            const int i0 = rt * R;
-            const int nr = min(R, r_count - i0);
+            const int i0 = rt * RT;
+            const int nr = min(RT, r_count - i0);
             float acc[V];
 #pragma unroll
             for (int t = 0; t < V; ++t) acc[t] = 0.f;
@@ -386,16 +403,25 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 
             warp_reduce_scatter<V>(acc, lane);
             const int idx = lane >> SH;
-            if ((lane & ((1 << SH) - 1)) == 0 && idx < nr * B) {
-                const int i = idx / B, b = idx - (idx / B) * B;
-                float tot = acc[0];
-                if (a.ktiles > 1) {
-                    float *cp = carry + (i0 + i) * B + b;
-                    if (kt > 0) tot += *cp;
-                    *cp = tot;
-                }
-                if (kt == a.ktiles - 1)
-                    store_y(mt.y, b * mt.ldy + r_begin + i0 + i, tot, a.y_f32 != 0);
+            const bool lead = (lane & ((1 << SH) - 1)) == 0;
+            // sums held: nr rows x B vectors, or for a pair the gate and the
+            // up sum of one row (index i = 0, 1) per vector
+            const int nsum = (a.pair ? 2 : nr) * B;
+            const int i = idx / B, b = idx - (idx / B) * B;
+            float tot = acc[0];
+            if (a.ktiles > 1 && lead && idx < nsum) {
+                float *cp = carry + ((a.pair ? 2 * i0 : i0) + i) * B + b;
+                if (kt > 0) tot += *cp;
+                *cp = tot;
+            }
+            if (R == 2 && a.pair) {
+                // the up sum of vector b sits B places further on
+                const float up = __shfl_sync(0xffffffffu, tot, ((idx + B) << SH) & 31);
+                if (kt == a.ktiles - 1 && lead && idx < B)
+                    store_y(mt.y, b * mt.ldy + r_begin + i0, tot / (1.0f + expf(-tot)) * up,
+                            a.y_f32 != 0);
+            } else if (kt == a.ktiles - 1 && lead && idx < nsum) {
+                store_y(mt.y, b * mt.ldy + r_begin + i0 + i, tot, a.y_f32 != 0);
             }
         }
     }
@@ -420,7 +446,7 @@ struct RowsPlan {
 // K in one launch and writes each matrix's first CTA to cta_begin[0..count].
 // max_warps caps the warps per CTA.
 bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
-               RowsPlan *out);
+               RowsPlan *out, bool pair = false);
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
                      int max_smem, int max_warps, RowsPlan *out, int *cta_begin);
 
@@ -456,7 +482,8 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     using P = Pattern<N, M>;
     const SpmvProblem &p0 = g.p[0];
     RowsArgs a = {};
-    for (int i = 0; i < g.count; ++i) {
+    const int nmat = g.pair ? 1 : g.count;  // a pair is one matrix entry (gate) plus up's arrays
+    for (int i = 0; i < nmat; ++i) {
         const SpmvProblem &p = g.p[i];
         RowsMat &m = a.mat[i];
         m.values = static_cast<const uint8_t *>(p.values);
@@ -469,8 +496,13 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
         m.row_base = static_cast<int>(p.rows / ctas);
         m.row_extra = static_cast<int>(p.rows % ctas);
     }
-    a.nmat = g.count;
-    a.cta_begin[g.count] = cta_begin[g.count];
+    if (g.pair) {
+        a.mat[0].values2 = static_cast<const uint8_t *>(g.p[1].values);
+        a.mat[0].masks2 = reinterpret_cast<const uint8_t *>(g.p[1].masks);
+    }
+    a.pair = g.pair ? 1 : 0;
+    a.nmat = nmat;
+    a.cta_begin[nmat] = cta_begin[nmat];
     a.err = p0.err;
     a.ldx = p0.ldx;
     a.vrow_bytes = p0.K / P::CK * 16;
@@ -497,7 +529,7 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     a.y_f32 = p0.y_f32 ? 1 : 0;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cta_begin[g.count]);
+    cfg.gridDim = dim3(cta_begin[nmat]);
     cfg.blockDim = dim3(32 * pl.W);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = s;
@@ -586,9 +618,11 @@ cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
     const int chunks = static_cast<int>(p0.K / P::CK);
     int64_t rows[kRowsMaxGroup];
     for (int i = 0; i < g.count; ++i) rows[i] = g.p[i].rows;
+    if (g.pair && (g.count != 2 || g.p[1].rows != p0.rows)) return cudaErrorNotSupported;
     auto plan = [&](int smem_cap, int max_warps) {
-        if (g.count == 1) {
-            if (!rows_plan(p0.rows, chunks, P::CK, p0.batch, nsm, smem_cap, max_warps, &pl))
+        if (g.count == 1 || g.pair) {
+            if (!rows_plan(p0.rows, chunks, P::CK, p0.batch, nsm, smem_cap, max_warps, &pl,
+                           g.pair))
                 return false;
             cta_begin[0] = 0;
             cta_begin[1] = pl.grid;

@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             L.nm_spmv_group.argtypes = [mp, i32, ctypes.POINTER(vp), i64, ctypes.POINTER(vp),
                                         ctypes.POINTER(i64), i32, i32, vp]
             L.nm_spmv_group.restype = ctypes.c_int
+            L.nm_spmv_gate_up_silu.argtypes = [mp, mp, vp, i64, vp, i64, i32, i32, vp]
+            L.nm_spmv_gate_up_silu.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -243,3 +245,22 @@ def nm_spmv_group(mats, xs, ys=None, y_dtype=torch.float16, stream=None):
                                      for y in ys])
     _check(lib().nm_spmv_group(descs, count, xp, ldx, yp, ldy, batch, yt, _stream(stream)))
     return ys
+
+
+def nm_spmv_gate_up_silu(gate: PackedMatrix, up: PackedMatrix, x: torch.Tensor,
+                         h: torch.Tensor | None = None, h_dtype=torch.float16,
+                         stream=None) -> torch.Tensor:
+    """h[b] = silu(gate x[b]) * (up x[b]) in one pass over both matrices;
+    x [K] or [batch][ldx] fp16, h [rows] or [batch][ldh]."""
+    _check_vec(x, "x")
+    vec = x.dim() == 1
+    batch = 1 if vec else x.shape[0]
+    ldx = x.shape[-1] if (vec or batch == 1) else x.stride(0)
+    if h is None:
+        h = torch.empty(gate.rows, dtype=h_dtype, device=x.device) if vec else \
+            torch.empty(batch, gate.rows, dtype=h_dtype, device=x.device)
+    ldh = h.stride(0) if (h.dim() > 1 and batch > 1) else h.shape[-1]
+    ht = NM_F32 if h.dtype == torch.float32 else NM_F16
+    _check(lib().nm_spmv_gate_up_silu(ctypes.byref(gate.desc), ctypes.byref(up.desc), _ptr(x),
+                                      ldx, _ptr(h), ldh, batch, ht, _stream(stream)))
+    return h

@@ -7,14 +7,16 @@ Decoding-Aware Pruning for Accurate and Efficient LLM Inference", Abstract).
 buffers, records the whole sequence once into a CUDA graph and replays it per
 token, so one graph launch replaces hundreds of host-side launches.  Layers
 that read the same input vector (the query, key and value projections; gate
-and up) can be fused into one ``nm_spmv_group`` launch.  Every launch is a
-libnm kernel; nothing else runs.
+and up) can be fused into one ``nm_spmv_group`` launch, and a gate/up pair
+into one ``nm_spmv_gate_up_silu`` launch that writes the gated MLP input
+silu(gate x) * (up x) in place of the two outputs.  Every launch is a libnm
+kernel; nothing else runs.
 """
 from __future__ import annotations
 
 import torch
 
-from .nm import PackedMatrix, nm_spmv, nm_spmv_batched, nm_spmv_group
+from .nm import PackedMatrix, nm_spmv, nm_spmv_batched, nm_spmv_gate_up_silu, nm_spmv_group
 
 
 def shared_input_groups(xs, mats):
@@ -33,17 +35,44 @@ def shared_input_groups(xs, mats):
 
 
 class LayerStream:
-    def __init__(self, mats, xs, ys, fuse_shared_input: bool = False):
+    def __init__(self, mats, xs, ys, fuse_shared_input: bool = False, silu_pairs=()):
         """mats: PackedMatrix list; xs[i]: fp16 [batch][K_i] (or [K_i]);
         ys[i]: fp16/fp32 [batch][rows_i] (or [rows_i]), preallocated.  With
         fuse_shared_input, consecutive layers passed the same x tensor are
-        computed by one grouped launch."""
+        computed by one grouped launch.  silu_pairs: (gate, up) index pairs of
+        consecutive layers with the same x and shape; each becomes one launch
+        writing silu(gate x) * (up x) into ys[gate] (ys[up] is not written)."""
         assert len(mats) == len(xs) == len(ys)
         self.mats = list(mats)
         self.xs = list(xs)
         self.ys = list(ys)
-        self.groups = (shared_input_groups(self.xs, self.mats) if fuse_shared_input
-                       else [[i] for i in range(len(self.mats))])
+        self.silu_pairs = {tuple(p) for p in silu_pairs}
+        for gi, ui in self.silu_pairs:
+            assert ui == gi + 1 and self.xs[gi] is self.xs[ui]
+        groups = (shared_input_groups(self.xs, self.mats) if fuse_shared_input
+                  else [[i] for i in range(len(self.mats))])
+        # a pair always takes its own launch
+        merged = []
+        for g in groups:  # unfused: join the pair's two single-layer groups
+            if (merged and len(g) == 1 and len(merged[-1]) == 1
+                    and (merged[-1][0], g[0]) in self.silu_pairs):
+                merged[-1] = [merged[-1][0], g[0]]
+            else:
+                merged.append(list(g))
+        self.groups = []
+        for g in merged:
+            rest = list(g)
+            while rest:
+                pair = next(((rest[k], rest[k + 1]) for k in range(len(rest) - 1)
+                             if (rest[k], rest[k + 1]) in self.silu_pairs), None)
+                if pair is None:
+                    self.groups.append(rest)
+                    break
+                k = rest.index(pair[0])
+                if rest[:k]:
+                    self.groups.append(rest[:k])
+                self.groups.append(list(pair))
+                rest = rest[k + 2:]
         self.graph = None
 
     def __len__(self):
@@ -55,6 +84,10 @@ class LayerStream:
 
     def run_eager(self, stream=None):
         for g in self.groups:
+            if len(g) == 2 and tuple(g) in self.silu_pairs:
+                nm_spmv_gate_up_silu(self.mats[g[0]], self.mats[g[1]], self.xs[g[0]],
+                                     self.ys[g[0]], stream=stream)
+                continue
             if len(g) > 1:
                 nm_spmv_group([self.mats[i] for i in g], [self.xs[i] for i in g],
                               [self.ys[i] for i in g], stream=stream)

@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_interface():
     assert {"nm_packed_sizes", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_batched",
-            "nm_device_errors", "nm_status_str", "nm_last_error",
-            "nm_version"} <= set(declared_functions())
+            "nm_spmv_group", "nm_spmv_gate_up_silu", "nm_device_errors", "nm_status_str",
+            "nm_last_error", "nm_version"} <= set(declared_functions())
 
 
 def test_spmv_group_checks_arguments_on_the_host():
@@ -54,6 +54,30 @@ def test_spmv_group_checks_arguments_on_the_host():
     xbad = (ctypes.c_void_p * 2)(C16, C16 + 2)
     st = L.nm_spmv_group(same, 2, xbad, 64, yp, None, 1, nm.NM_F16, None)
     assert st in (nm.NM_ERR_INVALID_ARG, nm.NM_ERR_CUDA)
+
+
+def test_gate_up_silu_checks_arguments_on_the_host():
+    L = nm.lib()
+    G = nm.nm_matrix(16, 128, 2, 4, A16, B16)
+    U_rows = nm.nm_matrix(8, 128, 2, 4, A16, B16)
+    U_pat = nm.nm_matrix(16, 128, 1, 4, A16, B16)
+    assert L.nm_spmv_gate_up_silu(ctypes.byref(G), ctypes.byref(U_rows), C16, 128, D16, 16, 1,
+                                  nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert "same rows" in nm.nm_last_error()
+    assert L.nm_spmv_gate_up_silu(ctypes.byref(G), ctypes.byref(U_pat), C16, 128, D16, 16, 1,
+                                  nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_gate_up_silu(None, ctypes.byref(G), C16, 128, D16, 16, 1, nm.NM_F16,
+                                  None) == nm.NM_ERR_INVALID_ARG
+    # per-matrix checks name the matrix: ldh < rows, batch out of range
+    assert L.nm_spmv_gate_up_silu(ctypes.byref(G), ctypes.byref(G), C16, 128, D16, 8, 1,
+                                  nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert nm.nm_last_error().startswith("gate")
+    assert L.nm_spmv_gate_up_silu(ctypes.byref(G), ctypes.byref(G), C16, 128, D16, 16, 0,
+                                  nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    # K not a multiple of 128: no streaming kernel, unsupported (before any launch)
+    G64 = nm.nm_matrix(16, 64, 2, 4, A16, B16)
+    assert L.nm_spmv_gate_up_silu(ctypes.byref(G64), ctypes.byref(G64), C16, 64, D16, 16, 1,
+                                  nm.NM_F16, None) == nm.NM_ERR_UNSUPPORTED
 
 
 def test_device_errors_rejects_null_on_the_host():
