@@ -68,6 +68,7 @@ def parse_args(argv=None):
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-prune", action="store_true", help="skip the mask-selection timing")
     return p.parse_args(argv)
 
 
@@ -394,6 +395,40 @@ def pair_pass(gate, up, batch, reps, l2_bytes):
     return out
 
 
+def prune_pass(wl, N, M, reps, l2_bytes):
+    """nm_select_mask and nm_prune_pack on the dense fp16 weights of the
+    block's largest layer, with an activation-norm column scale, each a CUDA
+    graph of calls rotating over > 3x L2 of weight copies.  Returns
+    {name: (seconds per call, algorithmic bytes per call)}."""
+    from sparse_spmv_memory_02_b300 import nm
+    li, layer = max(layer_list(wl)[:len(wl.layers)], key=lambda t: t[1].rows * t[1].K)
+    rows, K = layer.rows, layer.K
+    W0 = nm_synth.weights(rows, K, nm_synth.weight_seed(wl, li), "cuda")
+    ncopy = max(2, -(-3 * l2_bytes // W0.numel() // 2))
+    Ws = [W0] + [W0.clone() for _ in range(ncopy - 1)]
+    x = nm_synth.activations(K, 64, nm_synth.x_seed(wl, li), wl.outliers, "cuda")
+    scale = x.float().norm(dim=0).contiguous()  # column norms over 64 synthetic tokens
+    mask = torch.empty(rows, K, dtype=torch.uint8, device="cuda")
+    A = nm.nm_prune_pack(W0, N, M, scale)
+    n = max(reps // 5, ncopy)
+
+    def run_select():
+        for i in range(n):
+            nm.nm_select_mask(Ws[i % ncopy], N, M, scale, mask=mask)
+
+    def run_prune():
+        for i in range(n):
+            nm.nm_prune_pack(Ws[i % ncopy], N, M, scale, values=A.values, masks=A.masks)
+
+    wbytes = rows * K * 2 + K * 4
+    out = {"select_mask": (_graph_time(run_select, n), wbytes + rows * K),
+           "prune_pack": (_graph_time(run_prune, n), wbytes + A.nbytes),
+           "shape": (layer.name, rows, K)}
+    del Ws, W0, mask, A
+    torch.cuda.empty_cache()
+    return out
+
+
 def dense_pass(layers, copies, steps, warmup):
     """cuBLAS fp16 GEMV of W (dropped weights zeroed), same protocol."""
     n = len(layers)
@@ -638,6 +673,16 @@ def run_ours(args, world, rank, local):
                            "launch writing both outputs, or one nm_spmv_gate_up_silu launch "
                            "writing silu(gate x) * (up x)")
 
+    prune = None
+    if not args.no_prune:
+        pp = prune_pass(wl, N, M, args.profile_steps, l2_bytes)
+        name, prow, pk = pp.pop("shape")
+        prune = {k: {"us": t * 1e6, "bytes": b, "gbs": b / t / 1e9} for k, (t, b) in pp.items()}
+        prune["layer"] = {"name": name, "rows": prow, "K": pk}
+        prune["note"] = ("N:M selection from scores |w| * ||x_k|| (column norms of 64 synthetic "
+                         "tokens) on the block's largest layer: the u8 mask, or selection and "
+                         "pack in one pass; bytes = W read + scale + output written")
+
     dense = None
     if not args.no_dense:
         ddt, dbytes, _ = dense_pass(layers, copies, max(10, min(args.steps, 500)), args.warmup)
@@ -680,6 +725,9 @@ def run_ours(args, world, rank, local):
     if gate_up:
         for k in ("group", "silu"):
             gate_up[k]["frac_of_peak"] = gate_up[k]["gbs"] / peak
+    if prune:
+        for k in ("select_mask", "prune_pack"):
+            prune[k]["frac_of_peak"] = prune[k]["gbs"] / peak
     value = world * step_b * args.steps / dt / 1e9
     achieved = step_b * args.steps / dt / 1e9  # this rank's step: all launches are the SpMV kernel
     per_layer = {}
@@ -698,6 +746,7 @@ def run_ours(args, world, rank, local):
                             "packed copies",
         "per_layer": per_layer,
         "gate_up": gate_up,
+        "prune": prune,
         "step_algorithmic_bytes": step_b,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 120 /* 1.2.0 */
+#define NM_VERSION 130 /* 1.3.0 */
 #define NM_MAX_BATCH 8
 #define NM_MAX_GROUP 8
 
@@ -202,6 +202,38 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
                         void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
                         nm_stream_t stream);
+
+/*
+ * N:M keep-mask from scores, the step before nm_pack in a pruning flow.  In
+ * every group of M consecutive weights of a row keep the N of largest score
+ * s(r, k) = |W[r][k]| (col_scale NULL: magnitude pruning) or
+ * |W[r][k]| * col_scale[k] (a per-input-channel importance, e.g. the norm of
+ * input feature k over calibration activations: the activation-weighted
+ * magnitude of the Wanda family of training-free pruning methods, the
+ * baseline named by the bedrocknews summary of arXiv 2610.12327v1).  Scores
+ * are fp32: |w| is exact, the product rounds to nearest.  Position q of a
+ * group is kept iff fewer than N positions beat it, q' beating q when
+ * s(q') > s(q), or s(q') == s(q) and q' < q (ties go to the lower k), so
+ * exactly N are kept unless a score is NaN (then the group is unspecified).
+ *   W          fp16 [rows][K], device, 16-byte aligned; K % M == 0.
+ *   col_scale  fp32 [K], device, 16-byte aligned, or NULL.
+ *   mask       u8 [rows][K], device, 16-byte aligned; 1 = keep, 0 = drop
+ *              (the mask nm_pack takes).
+ * Errors: as nm_pack's shape checks; NM_ERR_INVALID_ARG for NULL or
+ * misaligned pointers.  Asynchronous, allocates nothing, capturable.
+ */
+nm_status nm_select_mask(const void *W, const float *col_scale, int64_t rows, int64_t K, int N,
+                         int M, uint8_t *mask, nm_stream_t stream);
+
+/*
+ * nm_select_mask and nm_pack in one pass over W: writes the packed layout
+ * (values, masks as for nm_pack) of W pruned by the same rule, without the
+ * u8 mask.  Same arguments and errors as nm_select_mask, values and masks as
+ * nm_pack (16-byte aligned).  Asynchronous, allocates nothing, capturable
+ * (unlike nm_pack it has no invalid groups to report).
+ */
+nm_status nm_prune_pack(const void *W, const float *col_scale, int64_t rows, int64_t K, int N,
+                        int M, void *values, uint32_t *masks, nm_stream_t stream);
 
 /*
  * The gated MLP input of a decoder layer in one pass over both weight

@@ -58,6 +58,8 @@ def _load(path: str | None = None):
                                                    vp, i64, vp, vp, i64, i64, i64]
             lib.oracle_spmv_packed_f64.restype = None
             lib.oracle_topn_mask.argtypes = [i64, i64, i32, i32, vp, vp]
+            lib.oracle_select_mask.argtypes = [i64, i64, i32, i32, vp, vp, vp]
+            lib.oracle_select_mask.restype = None
             lib.oracle_topn_mask.restype = None
             _lib = lib
     return _lib
@@ -179,6 +181,21 @@ def topn_mask(W, N: int, M: int) -> np.ndarray:
     rows, K = W.shape
     mask = np.empty((rows, K), dtype=np.uint8)
     _load().oracle_topn_mask(rows, K, N, M, _ptr(W), _ptr(mask))
+    return mask
+
+
+def select_mask(W, N: int, M: int, scale=None) -> np.ndarray:
+    """Keep the N largest scores of every group of M along K, score |w| or
+    |w| * scale[k] in fp32 (ties -> lower k)."""
+    W = _u16(W)
+    rows, K = W.shape
+    mask = np.empty((rows, K), dtype=np.uint8)
+    sp = None
+    if scale is not None:
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+        assert scale.shape == (K,)
+        sp = _ptr(scale)
+    _load().oracle_select_mask(rows, K, N, M, _ptr(W), sp, _ptr(mask))
     return mask
 
 

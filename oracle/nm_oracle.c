@@ -256,3 +256,43 @@ void oracle_topn_mask(int64_t rows, int64_t K, int N, int M,
         }
     }
 }
+
+/*
+ * Score-driven N:M keep-mask: the selection step before packing.  The score
+ * of weight (r, k) is |w| in single precision (exact for fp16) and, when
+ * scale is given, |w| * scale[k] rounded to single precision; scale is a
+ * per-input-channel importance (the activation-weighted magnitude of the
+ * Wanda family of pruning methods, the baseline named by the bedrocknews
+ * summary of arXiv 2610.12327v1).  Position q of a group is kept iff fewer
+ * than N positions beat it, q' beating q when s(q') > s(q), or
+ * s(q') == s(q) and q' < q.  With scale NULL this is oracle_topn_mask.
+ */
+void oracle_select_mask(int64_t rows, int64_t K, int N, int M, const uint16_t *W,
+                        const float *scale, uint8_t *mask)
+{
+    int64_t groups = K / M;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t g = 0; g < groups; ++g) {
+            float sc[8];
+            for (int q = 0; q < M; ++q) {
+                int64_t k = g * M + q;
+                float a = (float)fabs(oracle_half_to_double(W[r * K + k]));
+                if (scale) {
+                    volatile float prod = a * scale[k]; /* one rounding to single */
+                    a = prod;
+                }
+                sc[q] = a;
+            }
+            for (int q = 0; q < M; ++q) {
+                int beaten = 0;
+                for (int q2 = 0; q2 < M; ++q2) {
+                    if (q2 == q)
+                        continue;
+                    if (sc[q2] > sc[q] || (sc[q2] == sc[q] && q2 < q))
+                        ++beaten;
+                }
+                mask[r * K + g * M + q] = (uint8_t)(beaten < N ? 1 : 0);
+            }
+        }
+    }
+}

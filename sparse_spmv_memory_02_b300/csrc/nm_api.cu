@@ -349,6 +349,41 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx, void *
     return run_product(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+nm_status nm_select_mask(const void *W, const float *col_scale, int64_t rows, int64_t K, int N,
+                         int M, uint8_t *mask, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    nm_status st = check_shape(rows, K, N, M);
+    if (st != NM_OK) return st;
+    if (rows == 0 || K == 0) return NM_OK;
+    if (!W || !mask) return fail(NM_ERR_INVALID_ARG, "W and mask must be non-NULL");
+    if (!aligned(W, 16) || !aligned(mask, 16) || (col_scale && !aligned(col_scale, 16)))
+        return fail(NM_ERR_INVALID_ARG, "W, mask and col_scale must be 16-byte aligned");
+    const cudaError_t e = nm::launch_select(static_cast<const uint16_t *>(W), col_scale, rows, K,
+                                            N, M, mask, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "nm_select_mask launch");
+    return NM_OK;
+}
+
+nm_status nm_prune_pack(const void *W, const float *col_scale, int64_t rows, int64_t K, int N,
+                        int M, void *values, uint32_t *masks, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    nm_status st = check_shape(rows, K, N, M);
+    if (st != NM_OK) return st;
+    if (rows == 0 || K == 0) return NM_OK;
+    if (!W || !values || !masks)
+        return fail(NM_ERR_INVALID_ARG, "W, values and masks must be non-NULL");
+    if (!aligned(W, 16) || !aligned(values, 16) || !aligned(masks, 16) ||
+        (col_scale && !aligned(col_scale, 16)))
+        return fail(NM_ERR_INVALID_ARG, "W, values, masks and col_scale must be 16-byte aligned");
+    const cudaError_t e = nm::launch_prune_pack(static_cast<const uint16_t *>(W), col_scale, rows,
+                                                K, N, M, static_cast<uint16_t *>(values), masks,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "nm_prune_pack launch");
+    return NM_OK;
+}
+
 nm_status nm_spmv_gate_up_silu(const nm_matrix *gate, const nm_matrix *up, const void *x,
                                int64_t ldx, void *h, int64_t ldh, int batch, nm_dtype h_type,
                                nm_stream_t stream)

@@ -62,6 +62,14 @@ cudaError_t launch_pack(const uint16_t *W, const uint8_t *mask, int64_t rows, in
 cudaError_t launch_unpack(const uint16_t *values, const uint32_t *masks, int64_t rows,
                           int64_t K, int N, int M, uint16_t *W, cudaStream_t s);
 
+// N:M selection from scores |w| (scale null) or |w| * scale[k]: the keep-mask
+// (u8 [rows][K]), or the packed layout directly (nm_select.cu).  W, scale,
+// mask, values and masks 16-byte aligned; K % M == 0.
+cudaError_t launch_select(const uint16_t *W, const float *scale, int64_t rows, int64_t K, int N,
+                          int M, uint8_t *mask, cudaStream_t s);
+cudaError_t launch_prune_pack(const uint16_t *W, const float *scale, int64_t rows, int64_t K,
+                              int N, int M, uint16_t *values, uint32_t *masks, cudaStream_t s);
+
 // Cached device attributes of the current device.
 int sm_count();
 int max_dynamic_smem();

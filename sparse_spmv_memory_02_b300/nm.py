@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
             L.nm_spmv_group.restype = ctypes.c_int
             L.nm_spmv_gate_up_silu.argtypes = [mp, mp, vp, i64, vp, i64, i32, i32, vp]
             L.nm_spmv_gate_up_silu.restype = ctypes.c_int
+            L.nm_select_mask.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
+            L.nm_select_mask.restype = ctypes.c_int
+            L.nm_prune_pack.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp]
+            L.nm_prune_pack.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -264,3 +268,46 @@ def nm_spmv_gate_up_silu(gate: PackedMatrix, up: PackedMatrix, x: torch.Tensor,
     _check(lib().nm_spmv_gate_up_silu(ctypes.byref(gate.desc), ctypes.byref(up.desc), _ptr(x),
                                       ldx, _ptr(h), ldh, batch, ht, _stream(stream)))
     return h
+
+
+def nm_select_mask(W: torch.Tensor, N: int, M: int, col_scale: torch.Tensor | None = None,
+                   mask: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """u8 keep-mask [rows][K] keeping the N largest scores of every group of
+    M along K: |w|, or |w| * col_scale[k] (fp32 [K]) when given."""
+    if W.dtype != torch.float16 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous fp16 tensor")
+    rows, K = W.shape
+    if mask is None:
+        mask = torch.empty(rows, K, dtype=torch.uint8, device=W.device)
+    sp = None
+    if col_scale is not None:
+        if col_scale.dtype != torch.float32 or not col_scale.is_contiguous():
+            raise ValueError("col_scale must be a contiguous fp32 tensor")
+        sp = _ptr(col_scale)
+    _check(lib().nm_select_mask(_ptr(W), sp, rows, K, N, M, _ptr(mask), _stream(stream)))
+    return mask
+
+
+def nm_prune_pack(W: torch.Tensor, N: int, M: int, col_scale: torch.Tensor | None = None,
+                  values: torch.Tensor | None = None, masks: torch.Tensor | None = None,
+                  stream=None) -> PackedMatrix:
+    """nm_select_mask and nm_pack in one pass: the packed matrix of W pruned
+    to N:M by score |w| or |w| * col_scale[k]."""
+    if W.dtype != torch.float16 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous fp16 tensor")
+    rows, K = W.shape
+    vb, mb = nm_packed_sizes(rows, K, N, M)
+    if values is None:
+        values = torch.empty(vb // 2, dtype=torch.float16, device=W.device).view(rows, -1) \
+            if rows else torch.empty(0, (K // M) * N, dtype=torch.float16, device=W.device)
+    if masks is None:
+        masks = torch.empty(mb // 4, dtype=torch.int32, device=W.device).view(rows, -1) \
+            if rows else torch.empty(0, (K + 31) // 32, dtype=torch.int32, device=W.device)
+    sp = None
+    if col_scale is not None:
+        if col_scale.dtype != torch.float32 or not col_scale.is_contiguous():
+            raise ValueError("col_scale must be a contiguous fp32 tensor")
+        sp = _ptr(col_scale)
+    _check(lib().nm_prune_pack(_ptr(W), sp, rows, K, N, M, _ptr(values), _ptr(masks),
+                               _stream(stream)))
+    return PackedMatrix(values, masks, rows, K, N, M)

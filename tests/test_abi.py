@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_interface():
     assert {"nm_packed_sizes", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_batched",
-            "nm_spmv_group", "nm_spmv_gate_up_silu", "nm_device_errors", "nm_status_str",
+            "nm_spmv_group", "nm_spmv_gate_up_silu", "nm_select_mask", "nm_prune_pack",
+            "nm_device_errors", "nm_status_str",
             "nm_last_error", "nm_version"} <= set(declared_functions())
 
 
@@ -78,6 +79,17 @@ def test_gate_up_silu_checks_arguments_on_the_host():
     G64 = nm.nm_matrix(16, 64, 2, 4, A16, B16)
     assert L.nm_spmv_gate_up_silu(ctypes.byref(G64), ctypes.byref(G64), C16, 64, D16, 16, 1,
                                   nm.NM_F16, None) == nm.NM_ERR_UNSUPPORTED
+
+
+def test_select_and_prune_pack_check_arguments_on_the_host():
+    L = nm.lib()
+    for f, extra in ((L.nm_select_mask, (D16,)), (L.nm_prune_pack, (D16, D16 + 4096))):
+        assert f(None, None, 16, 64, 2, 4, *extra, None) == nm.NM_ERR_INVALID_ARG
+        assert f(A16 + 2, None, 16, 64, 2, 4, *extra, None) == nm.NM_ERR_INVALID_ARG
+        assert f(A16, B16 + 4, 16, 64, 2, 4, *extra, None) == nm.NM_ERR_INVALID_ARG
+        assert f(A16, None, 16, 64, 2, 3, *extra, None) == nm.NM_ERR_UNSUPPORTED
+        assert f(A16, None, 16, 62, 2, 4, *extra, None) == nm.NM_ERR_INVALID_ARG
+        assert f(None, None, 0, 64, 2, 4, *extra, None) == nm.NM_OK  # nothing to do
 
 
 def test_device_errors_rejects_null_on_the_host():
