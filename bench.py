@@ -69,6 +69,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-prune", action="store_true", help="skip the mask-selection timing")
+    p.add_argument("--no-calib", action="store_true", help="skip the calibration timing")
+    p.add_argument("--calib-tokens", type=int, default=512,
+                   help="decode-step tokens per nm_calib_accumulate call in the calibration timing")
     return p.parse_args(argv)
 
 
@@ -82,6 +85,18 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tc_peak():
+    """Dense fp16 tensor peak in TFLOP/s: the measured cuBLAS bf16 burst figure
+    (fp16 and bf16 share one rate), else the profiling fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured (bf16 burst; fp16 runs at the same rate)"
+    except Exception:
+        return 1800.0, "fallback"
 
 
 def host_cores():
@@ -429,6 +444,28 @@ def prune_pass(wl, N, M, reps, l2_bytes):
     return out
 
 
+def calib_pass(wl, tokens, reps):
+    """nm_calib_accumulate (H += X^T X on the tensor cores) for `tokens`
+    decode-step inputs of each distinct layer-input width of the block.
+    Returns {K: (seconds per call, flops, bytes)}: flops 2 T K^2; bytes the
+    read-modify-write of H (8 K^2) plus X once."""
+    from sparse_spmv_memory_02_b300 import nm
+    out = {}
+    for K in sorted({layer.K for layer in wl.layers}):
+        X = nm_synth.activations(K, tokens, 77 + K, wl.outliers, "cuda")
+        H = torch.zeros(K, K, dtype=torch.float32, device="cuda")
+        n = max(3, reps // 10)
+
+        def run():
+            for _ in range(n):
+                nm.nm_calib_accumulate(X, H)
+        t = _graph_time(run, n)
+        out[K] = (t, 2.0 * tokens * K * K, 8.0 * K * K + 2.0 * tokens * K)
+        del X, H
+        torch.cuda.empty_cache()
+    return out
+
+
 def dense_pass(layers, copies, steps, warmup):
     """cuBLAS fp16 GEMV of W (dropped weights zeroed), same protocol."""
     n = len(layers)
@@ -683,6 +720,16 @@ def run_ours(args, world, rank, local):
                          "tokens) on the block's largest layer: the u8 mask, or selection and "
                          "pack in one pass; bytes = W read + scale + output written")
 
+    calib = None
+    if not args.no_calib:
+        cp = calib_pass(wl, args.calib_tokens, args.profile_steps)
+        calib = {"tokens": args.calib_tokens,
+                 "note": "nm_calib_accumulate: H += X^T X over decode-step layer inputs "
+                         "(fp16 X, fp32 H) on tcgen05 tensor cores, per distinct input width K; "
+                         "flops 2 T K^2, bytes H read+write + X"}
+        for K, (t, fl, by) in cp.items():
+            calib["K%d" % K] = {"us": t * 1e6, "tflops": fl / t / 1e12, "gbs": by / t / 1e9}
+
     dense = None
     if not args.no_dense:
         ddt, dbytes, _ = dense_pass(layers, copies, max(10, min(args.steps, 500)), args.warmup)
@@ -728,6 +775,14 @@ def run_ours(args, world, rank, local):
     if prune:
         for k in ("select_mask", "prune_pack"):
             prune[k]["frac_of_peak"] = prune[k]["gbs"] / peak
+    if calib:
+        tc_peak, tc_kind = measured_tc_peak()
+        for k, v in calib.items():
+            if k.startswith("K"):
+                v["frac_of_tensor_peak"] = v["tflops"] / tc_peak
+                v["frac_of_hbm_peak"] = v["gbs"] / peak
+        calib["tensor_peak_tflops"] = tc_peak
+        calib["tensor_peak_kind"] = tc_kind
     value = world * step_b * args.steps / dt / 1e9
     achieved = step_b * args.steps / dt / 1e9  # this rank's step: all launches are the SpMV kernel
     per_layer = {}
@@ -747,6 +802,7 @@ def run_ours(args, world, rank, local):
         "per_layer": per_layer,
         "gate_up": gate_up,
         "prune": prune,
+        "calib": calib,
         "step_algorithmic_bytes": step_b,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 130 /* 1.3.0 */
+#define NM_VERSION 140 /* 1.4.0 */
 #define NM_MAX_BATCH 8
 #define NM_MAX_GROUP 8
 
@@ -202,6 +202,27 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
                         void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
                         nm_stream_t stream);
+
+/*
+ * Decode-only calibration accumulation: H[i][j] += sum_t X[t][i] * X[t][j]
+ * for i, j < K, t < T.  SparseDecoding builds each layer's pruning
+ * calibration matrix from the layer inputs collected while the dense model
+ * generates, the prefill excluded ("SparseDecoding: Decoding-Aware Pruning
+ * for Accurate and Efficient LLM Inference", Abstract); the caller passes
+ * only decode-step activations, batch by batch, and H accumulates X^T X.
+ * Runs on the tensor cores (fp16 products exact, fp32 sums; H is added to
+ * with fp32 reductions, so concurrent calls on one H add up, in an
+ * unspecified order).
+ *   X    fp16 [T][ldx], device, 16-byte aligned; K % 8 == 0, ldx >= K and a
+ *        multiple of 8.
+ *   H    fp32 [K][ldh], device, 16-byte aligned; ldh >= K, multiple of 4.
+ * Errors: NM_ERR_INVALID_ARG for bad sizes, strides or pointers;
+ * NM_ERR_UNSUPPORTED if the driver has no tensor-map encoder; NM_ERR_CUDA.
+ * Asynchronous, allocates nothing, may be captured in a CUDA graph (the
+ * call's tensor map is built on the host at call time).
+ */
+nm_status nm_calib_accumulate(const void *X, int64_t T, int64_t K, int64_t ldx, float *H,
+                              int64_t ldh, nm_stream_t stream);
 
 /*
  * N:M keep-mask from scores, the step before nm_pack in a pruning flow.  In

@@ -60,6 +60,8 @@ def _load(path: str | None = None):
             lib.oracle_topn_mask.argtypes = [i64, i64, i32, i32, vp, vp]
             lib.oracle_select_mask.argtypes = [i64, i64, i32, i32, vp, vp, vp]
             lib.oracle_select_mask.restype = None
+            lib.oracle_calib_f64.argtypes = [i64, i64, vp, i64, vp, vp]
+            lib.oracle_calib_f64.restype = None
             lib.oracle_topn_mask.restype = None
             _lib = lib
     return _lib
@@ -197,6 +199,25 @@ def select_mask(W, N: int, M: int, scale=None) -> np.ndarray:
         sp = _ptr(scale)
     _load().oracle_select_mask(rows, K, N, M, _ptr(W), sp, _ptr(mask))
     return mask
+
+
+def calib_accumulate(X, H0=None):
+    """fp64 reference of H0 + X^T X (X fp16 [T][K]) and S = sum_t |x_ti x_tj|.
+    Returns (H, S), both [K][K] float64."""
+    X = _u16(X)
+    T, K = X.shape
+    H = np.zeros((K, K)) if H0 is None else np.array(H0, dtype=np.float64, copy=True)
+    S = np.empty((K, K))
+    _load().oracle_calib_f64(T, K, _ptr(X), K, _ptr(H), _ptr(S))
+    return H, S
+
+
+def calib_within_tolerance(H_gpu, H_ref, S, rel: float = 1e-3):
+    """|H - H_ref| <= rel * S + 2**-22 |H_ref| + 1e-6: the products are exact
+    in fp32, the sums over tokens carry fp32 rounding (bounded by rel * S),
+    and adding to an existing H rounds once more."""
+    H_gpu = np.asarray(H_gpu, dtype=np.float64)
+    return np.abs(H_gpu - H_ref) <= rel * S + 2.0 ** -22 * np.abs(H_ref) + 1e-6
 
 
 def silu(g):

@@ -296,3 +296,29 @@ void oracle_select_mask(int64_t rows, int64_t K, int N, int M, const uint16_t *W
         }
     }
 }
+
+/*
+ * Decode-only calibration accumulation, the layer statistic SparseDecoding
+ * collects while the dense model generates ("SparseDecoding: Decoding-Aware
+ * Pruning for Accurate and Efficient LLM Inference", Abstract):
+ * H[i][j] += sum_t x_t[i] x_t[j] over the T token rows of X (fp16 [T][ldx]),
+ * in fp64; S[i][j] (if given) receives sum_t |x_t[i] x_t[j]| for the
+ * tolerance.  H and S are [K][K].
+ */
+void oracle_calib_f64(int64_t T, int64_t K, const uint16_t *X, int64_t ldx, double *H, double *S)
+{
+    for (int64_t i = 0; i < K; ++i) {
+        for (int64_t j = 0; j < K; ++j) {
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t t = 0; t < T; ++t) {
+                double p = oracle_half_to_double(X[t * ldx + i]) *
+                           oracle_half_to_double(X[t * ldx + j]);
+                acc += p;
+                sabs += fabs(p);
+            }
+            H[i * K + j] += acc;
+            if (S)
+                S[i * K + j] = sabs;
+        }
+    }
+}

@@ -349,6 +349,36 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx, void *
     return run_product(p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+nm_status nm_calib_accumulate(const void *X, int64_t T, int64_t K, int64_t ldx, float *H,
+                              int64_t ldh, nm_stream_t stream)
+{
+    g_last_error[0] = 0;
+    if (T < 0 || K < 0) return fail(NM_ERR_INVALID_ARG, "negative size T=%lld K=%lld",
+                                    (long long)T, (long long)K);
+    if (T == 0 || K == 0) return NM_OK;
+    if (T > INT_MAX || K > (1 << 20))
+        return fail(NM_ERR_INVALID_ARG, "size too large T=%lld K=%lld", (long long)T,
+                    (long long)K);
+    if (K % 8 != 0) return fail(NM_ERR_INVALID_ARG, "K=%lld must be a multiple of 8", (long long)K);
+    if (ldx < K || ldx % 8 != 0)
+        return fail(NM_ERR_INVALID_ARG, "ldx=%lld must be >= K and a multiple of 8", (long long)ldx);
+    if (ldh < K || ldh % 4 != 0)
+        return fail(NM_ERR_INVALID_ARG, "ldh=%lld must be >= K and a multiple of 4", (long long)ldh);
+    if (!X || !H) return fail(NM_ERR_INVALID_ARG, "X and H must be non-NULL");
+    if (!aligned(X, 16) || !aligned(H, 16))
+        return fail(NM_ERR_INVALID_ARG, "X and H must be 16-byte aligned");
+    unsigned int *err = nullptr;
+    cudaError_t e = device_error_word(&err);
+    if (e != cudaSuccess) return cuda_fail(e, "nm_calib_accumulate: device error word");
+    e = nm::launch_calib(static_cast<const uint16_t *>(X), T, K, ldx, H, ldh, err,
+                         nm::calib_idesc(), nm::calib_desc_hi(8192, 1024),
+                         reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported)
+        return fail(NM_ERR_UNSUPPORTED, "nm_calib_accumulate: no tensor-map encoder in the driver");
+    if (e != cudaSuccess) return cuda_fail(e, "nm_calib_accumulate launch");
+    return NM_OK;
+}
+
 nm_status nm_select_mask(const void *W, const float *col_scale, int64_t rows, int64_t K, int N,
                          int M, uint8_t *mask, nm_stream_t stream)
 {

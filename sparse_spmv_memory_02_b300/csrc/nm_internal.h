@@ -70,6 +70,16 @@ cudaError_t launch_select(const uint16_t *W, const float *scale, int64_t rows, i
 cudaError_t launch_prune_pack(const uint16_t *W, const float *scale, int64_t rows, int64_t K,
                               int N, int M, uint16_t *values, uint32_t *masks, cudaStream_t s);
 
+// H[i][j] += sum_t X[t][i] X[t][j] on the tensor cores (nm_calib.cu); X fp16
+// [T][ldx] with K % 8 == 0, H fp32 [K][ldh] with ldh % 4 == 0, both 16-byte
+// aligned.  idesc / desc_hi: the MMA instruction descriptor and the operands'
+// shared-memory descriptor fields (calib_idesc(), calib_desc_hi(8192, 1024)).
+cudaError_t launch_calib(const uint16_t *X, int64_t T, int64_t K, int64_t ldx, float *H,
+                         int64_t ldh, unsigned int *err, uint32_t idesc, uint64_t desc_hi,
+                         cudaStream_t s);
+uint32_t calib_idesc();
+uint64_t calib_desc_hi(uint32_t lbo, uint32_t sbo);
+
 // Cached device attributes of the current device.
 int sm_count();
 int max_dynamic_smem();

@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
             L.nm_spmv_group.restype = ctypes.c_int
             L.nm_spmv_gate_up_silu.argtypes = [mp, mp, vp, i64, vp, i64, i32, i32, vp]
             L.nm_spmv_gate_up_silu.restype = ctypes.c_int
+            L.nm_calib_accumulate.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+            L.nm_calib_accumulate.restype = ctypes.c_int
             L.nm_select_mask.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
             L.nm_select_mask.restype = ctypes.c_int
             L.nm_prune_pack.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp]
@@ -311,3 +313,18 @@ def nm_prune_pack(W: torch.Tensor, N: int, M: int, col_scale: torch.Tensor | Non
     _check(lib().nm_prune_pack(_ptr(W), sp, rows, K, N, M, _ptr(values), _ptr(masks),
                                _stream(stream)))
     return PackedMatrix(values, masks, rows, K, N, M)
+
+
+def nm_calib_accumulate(X: torch.Tensor, H: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """H += X^T X for fp16 X [T][K] (decode-step layer inputs) into fp32 H
+    [K][K] (created zeroed if not given), on the tensor cores."""
+    if X.dtype != torch.float16 or X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be fp16 [T][K] with unit column stride")
+    T, K = X.shape
+    if H is None:
+        H = torch.zeros(K, K, dtype=torch.float32, device=X.device)
+    if H.dtype != torch.float32 or H.dim() != 2 or H.stride(1) != 1:
+        raise ValueError("H must be fp32 [K][ldh] with unit column stride")
+    ldx = X.stride(0) if T > 1 else K
+    _check(lib().nm_calib_accumulate(_ptr(X), T, K, ldx, _ptr(H), H.stride(0), _stream(stream)))
+    return H

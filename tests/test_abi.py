@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_interface():
     assert {"nm_packed_sizes", "nm_pack", "nm_unpack", "nm_spmv", "nm_spmv_batched",
             "nm_spmv_group", "nm_spmv_gate_up_silu", "nm_select_mask", "nm_prune_pack",
+            "nm_calib_accumulate",
             "nm_device_errors", "nm_status_str",
             "nm_last_error", "nm_version"} <= set(declared_functions())
 
@@ -90,6 +91,19 @@ def test_select_and_prune_pack_check_arguments_on_the_host():
         assert f(A16, None, 16, 64, 2, 3, *extra, None) == nm.NM_ERR_UNSUPPORTED
         assert f(A16, None, 16, 62, 2, 4, *extra, None) == nm.NM_ERR_INVALID_ARG
         assert f(None, None, 0, 64, 2, 4, *extra, None) == nm.NM_OK  # nothing to do
+
+
+def test_calib_accumulate_checks_arguments_on_the_host():
+    L = nm.lib()
+    assert L.nm_calib_accumulate(A16, 0, 64, 64, B16, 64, None) == nm.NM_OK  # no tokens
+    assert L.nm_calib_accumulate(A16, 4, 0, 64, B16, 64, None) == nm.NM_OK
+    assert L.nm_calib_accumulate(A16, -1, 64, 64, B16, 64, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_calib_accumulate(A16, 4, 60, 64, B16, 64, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_calib_accumulate(A16, 4, 64, 60, B16, 64, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_calib_accumulate(A16, 4, 64, 68, B16, 64, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_calib_accumulate(A16, 4, 64, 64, B16, 62, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_calib_accumulate(None, 4, 64, 64, B16, 64, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_calib_accumulate(A16 + 8, 4, 64, 64, B16, 64, None) == nm.NM_ERR_INVALID_ARG
 
 
 def test_device_errors_rejects_null_on_the_host():
