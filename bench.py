@@ -70,6 +70,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-prune", action="store_true", help="skip the mask-selection timing")
     p.add_argument("--no-calib", action="store_true", help="skip the calibration timing")
+    p.add_argument("--no-crossover", action="store_true",
+                   help="skip the batch crossover against 2:4 sparse tensor cores")
     p.add_argument("--calib-tokens", type=int, default=512,
                    help="decode-step tokens per nm_calib_accumulate call in the calibration timing")
     return p.parse_args(argv)
@@ -466,6 +468,77 @@ def calib_pass(wl, tokens, reps):
     return out
 
 
+def _eager_time(run, n, warmup=3):
+    """Median seconds per call of `run` (n calls per sample), launched
+    eagerly (library calls that may not be graph-capturable)."""
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(5):
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3 / n)
+    return statistics.median(times)
+
+
+def crossover_pass(batches=(1, 2, 4, 8, 16, 32, 64)):
+    """The batch at which a 2:4 sparse-tensor-core GEMM (cuSPARSELt through
+    torch's semi-structured sparse tensors, a library comparator) overtakes
+    this library's bandwidth kernel, on the Llama-3.3-70B-shaped gate layer
+    (28672 x 8192, 2:4): microseconds per product for libnm (batch <= 8),
+    the sparse tensor cores and dense cuBLAS on the masked weights, all
+    launched eagerly."""
+    from sparse_spmv_memory_02_b300 import nm
+    rows, K = 28672, 8192
+    W = nm_synth.weights(rows, K, 4242, "cuda")
+    mask = nm_synth.topn_mask(W, 2, 4)
+    A = nm.nm_pack(W, mask, 2, 4)
+    Wm = torch.where(mask.bool(), W, torch.zeros((), dtype=W.dtype, device="cuda"))
+    del W, mask
+    Ws, sparse_note = None, "cuSPARSELt 2:4 via torch.sparse.to_sparse_semi_structured"
+    try:
+        from torch.sparse import to_sparse_semi_structured
+        Ws = to_sparse_semi_structured(Wm)
+    except Exception as e:  # reported, not fatal: a comparator only
+        sparse_note = "unavailable: %s" % str(e).splitlines()[0][:160]
+    table = []
+    n = 10
+    for B in batches:
+        X = nm_synth.activations(K, B, 900 + B, True, "cuda")
+        Xt = X.t().contiguous()
+        row = {"batch": B}
+        if B <= nm.NM_MAX_BATCH:
+            y = torch.empty(B, rows, dtype=torch.float16, device="cuda")
+
+            def ours():
+                for _ in range(n):
+                    nm.nm_spmv_batched(A, X, y)
+            row["libnm_us"] = _eager_time(ours, n) * 1e6
+
+        def dense():
+            for _ in range(n):
+                torch.mm(Wm, Xt)
+        row["dense_cublas_us"] = _eager_time(dense, n) * 1e6
+        if Ws is not None:
+            try:
+                def sparse():
+                    for _ in range(n):
+                        torch.mm(Ws, Xt)
+                row["sparse_tc_us"] = _eager_time(sparse, n) * 1e6
+            except Exception as e:
+                row["sparse_tc_us"] = None
+                row["sparse_tc_error"] = str(e).splitlines()[0][:160]
+        table.append(row)
+    del A, Wm, Ws
+    torch.cuda.empty_cache()
+    return {"layer": {"rows": rows, "K": K, "pattern": "2:4"}, "sparse_tc": sparse_note,
+            "table": table}
+
+
 def dense_pass(layers, copies, steps, warmup):
     """cuBLAS fp16 GEMV of W (dropped weights zeroed), same protocol."""
     n = len(layers)
@@ -720,6 +793,10 @@ def run_ours(args, world, rank, local):
                          "tokens) on the block's largest layer: the u8 mask, or selection and "
                          "pack in one pass; bytes = W read + scale + output written")
 
+    crossover = None
+    if not args.no_crossover:
+        crossover = crossover_pass()
+
     calib = None
     if not args.no_calib:
         cp = calib_pass(wl, args.calib_tokens, args.profile_steps)
@@ -803,6 +880,7 @@ def run_ours(args, world, rank, local):
         "gate_up": gate_up,
         "prune": prune,
         "calib": calib,
+        "crossover": crossover,
         "step_algorithmic_bytes": step_b,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,
