@@ -449,8 +449,10 @@ def prune_pass(wl, N, M, reps, l2_bytes):
 def calib_pass(wl, tokens, reps):
     """nm_calib_accumulate (H += X^T X on the tensor cores) for `tokens`
     decode-step inputs of each distinct layer-input width of the block.
-    Returns {K: (seconds per call, flops, bytes)}: flops 2 T K^2; bytes the
-    read-modify-write of H (8 K^2) plus X once."""
+    Returns {K: (seconds per call, flops, bytes)}: flops T K (K + 1), the
+    symmetric rank-T update's count (the kernel computes the tiles on and
+    above the diagonal and mirrors them); bytes the read-modify-write of H
+    (8 K^2) plus X once."""
     from sparse_spmv_memory_02_b300 import nm
     out = {}
     for K in sorted({layer.K for layer in wl.layers}):
@@ -462,7 +464,7 @@ def calib_pass(wl, tokens, reps):
             for _ in range(n):
                 nm.nm_calib_accumulate(X, H)
         t = _graph_time(run, n)
-        out[K] = (t, 2.0 * tokens * K * K, 8.0 * K * K + 2.0 * tokens * K)
+        out[K] = (t, float(tokens) * K * (K + 1), 8.0 * K * K + 2.0 * tokens * K)
         del X, H
         torch.cuda.empty_cache()
     return out
@@ -803,7 +805,8 @@ def run_ours(args, world, rank, local):
         calib = {"tokens": args.calib_tokens,
                  "note": "nm_calib_accumulate: H += X^T X over decode-step layer inputs "
                          "(fp16 X, fp32 H) on tcgen05 tensor cores, per distinct input width K; "
-                         "flops 2 T K^2, bytes H read+write + X"}
+                         "flops T K (K+1) (symmetric update: tiles on and above the diagonal, "
+                         "mirrored), bytes H read+write + X"}
         for K, (t, fl, by) in cp.items():
             calib["K%d" % K] = {"us": t * 1e6, "tflops": fl / t / 1e12, "gbs": by / t / 1e9}
 

@@ -12,7 +12,8 @@
 //
 // It is a dense contraction over tokens, so it runs on tcgen05.mma (fp16
 // operands, fp32 accumulator in tensor memory):
-//   * one CTA per 128 x 128 tile of H; 4 warps;
+//   * one CTA per 128 x 128 tile of H on or above the diagonal (H is
+//     symmetric; the CTA also adds its tile's transpose below it); 4 warps;
 //   * warp 0 lane 0 streams 64-token slabs of X with TMA: for the tile's
 //     rows i0..i0+127 and columns j0..j0+127 the slab X[t0:t0+64][i0:i0+128]
 //     (operand A) and X[t0:t0+64][j0:j0+128] (operand B), each as two
@@ -22,9 +23,10 @@
 //     and X is token-major in memory) and commits each stage back to the
 //     producer;
 //   * all four warps read the accumulator out of tensor memory (warp w owns
-//     lanes 32w..32w+31, i.e. rows i0+32w..) and add it into H with vector
-//     reductions (red.global.add.v4.f32), so H is read-modified-written once
-//     per call and never re-read by the kernel.
+//     lanes 32w..32w+31, i.e. rows i0+32w..), stage it in shared memory and
+//     add it and its transpose into H with coalesced reductions
+//     (red.global.add.f32), so each element of H is read-modified-written
+//     once per call and never re-read by the kernel.
 // Every mbarrier wait is bounded (nm_pipe.cuh): a stalled pipeline sets the
 // error word, drains what it issued and releases its tensor memory.
 #include <cuda.h>
@@ -113,11 +115,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+__device__ __forceinline__ void red_add(float *p, float v)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 __global__ void __launch_bounds__(128, 2)
@@ -134,7 +134,14 @@ nm_calib_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
     volatile int *failed = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ti = blockIdx.x / a.tiles_per_row, tj = blockIdx.x - ti * a.tiles_per_row;
+    // H is symmetric: CTA b takes the b-th tile (ti, tj) with tj >= ti in
+    // row-major order and also adds its transpose to tile (tj, ti).
+    int ti = 0, rem = static_cast<int>(blockIdx.x);
+    while (rem >= a.tiles_per_row - ti) {
+        rem -= a.tiles_per_row - ti;
+        ++ti;
+    }
+    const int tj = ti + rem;
     const int i0 = ti * kTile, j0 = tj * kTile;
     const int nslab = (a.T + kSlab - 1) / kSlab;
 
@@ -211,20 +218,36 @@ nm_calib_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
     // tcgen05.ld is warp-wide: the decision to read out must be uniform
     const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_bar, 0)) != 0;
     if (!ok && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
-    const bool go = ok && __all_sync(0xffffffffu, *failed == 0) != 0 && nslab > 0;
+    // the same decision in every warp: the staging below has CTA barriers
+    const bool go = __syncthreads_and(ok && *failed == 0 && nslab > 0) != 0;
     tc_fence_after();
     if (go) {
-        const int row = i0 + 32 * warp + lane;
+        // The tile goes through shared memory (the stages are free: every
+        // TMA load has landed and every MMA has read its operands), rows
+        // padded to 129 floats, so that both H[i0 + r][j0 + c] and the
+        // mirrored H[j0 + c][i0 + r] are added with coalesced reductions
+        // (32 consecutive floats of H per warp instruction) and without bank
+        // conflicts on either side.
+        float *stg = reinterpret_cast<float *>(smem);
+        constexpr int kPitch = kTile + 1;
+        const int r = 32 * warp + lane;
 #pragma unroll 1
         for (int c0 = 0; c0 < kTile; c0 += 32) {
             float v[32];
             tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, v);
-            if (row < a.K) {
-                float *hp = a.H + static_cast<int64_t>(row) * a.ldh + j0 + c0;
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (j0 + c0 + 4 * q < a.K)
-                        red_add_v4(hp + 4 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 32; ++q) stg[r * kPitch + c0 + q] = v[q];
+        }
+        __syncthreads();
+        for (int rr = warp; rr < kTile && i0 + rr < a.K; rr += 4) {
+            float *hp = a.H + static_cast<int64_t>(i0 + rr) * a.ldh + j0;
+            for (int c = lane; c < kTile && j0 + c < a.K; c += 32) red_add(hp + c, stg[rr * kPitch + c]);
+        }
+        if (tj != ti) {
+            for (int c = warp; c < kTile && j0 + c < a.K; c += 4) {
+                float *hp = a.H + static_cast<int64_t>(j0 + c) * a.ldh + i0;
+                for (int rr = lane; rr < kTile && i0 + rr < a.K; rr += 32)
+                    red_add(hp + rr, stg[rr * kPitch + c]);
             }
         }
     }
@@ -313,7 +336,7 @@ cudaError_t launch_calib(const uint16_t *X, int64_t T, int64_t K, int64_t ldx, f
     a.idesc = idesc;
     a.desc_hi = desc_hi;
     a.err = err;
-    const int64_t tiles = static_cast<int64_t>(a.tiles_per_row) * a.tiles_per_row;
+    const int64_t tiles = static_cast<int64_t>(a.tiles_per_row) * (a.tiles_per_row + 1) / 2;
     if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
     nm_calib_kernel<<<static_cast<unsigned int>(tiles), 128, kSmemBytes, s>>>(map, a);
     return cudaGetLastError();
