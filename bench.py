@@ -770,6 +770,16 @@ def run_ours(args, world, rank, local):
                            "us_per_step": odt / args.steps * 1e6,
                            "value": variant_bytes[k] * args.steps / odt / 1e9}
 
+    # end to end right after the device-timed steps, before the other legs
+    e2e = None
+    if not args.no_e2e:
+        et, h2d, d2h = e2e_pass(layers, streams, copies, max(10, min(args.steps, 500)),
+                                args.warmup, args.batch)
+        e2e = {"value": step_b / et / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "us_per_step": et * 1e6,
+               "path": "pinned host x -> device, the step's graph (%s), y -> pinned host, "
+                       "host waits each step" % args.launch}
+
     # each layer alone, L2-cold, for the per-layer figures
     l2_bytes = l2
     first_block = layers[:len(wl.layers)]
@@ -820,15 +830,6 @@ def run_ours(args, world, rank, local):
         for L in layers:
             L["dense"] = None
         torch.cuda.empty_cache()
-
-    e2e = None
-    if not args.no_e2e:
-        et, h2d, d2h = e2e_pass(layers, streams, copies, max(10, min(args.steps, 500)),
-                                args.warmup, args.batch)
-        e2e = {"value": step_b / et / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "us_per_step": et * 1e6,
-               "path": "pinned host x -> device, the step's graph (%s), y -> pinned host, "
-                       "host waits each step" % args.launch}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
