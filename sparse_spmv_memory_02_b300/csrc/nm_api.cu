@@ -232,7 +232,15 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
 nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    if (nm::bulk_path_applies(p.N, p.M, p.K)) {
+    // 2:4 at batch 8 on layers with more than 128 rows an SM: the tensor-core
+    // product (the CUDA-core kernel is instruction-bound there)
+    uint32_t tc_lbo = 0;
+    const int tc = nm::spmm_tc_mode(&tc_lbo);
+    const int nsm = nm::sm_count();
+    if (tc != 0 && nm::spmm_tc_applies(p, nsm) &&
+        (tc == 1 || (p.batch == 8 && p.rows > 128LL * nsm)))
+        e = nm::launch_spmm_tc(p, nm::spmm_tc_desc_hi(tc_lbo), s);
+    if (e == cudaErrorNotSupported && nm::bulk_path_applies(p.N, p.M, p.K)) {
         nm::SpmvGroup g;
         g.count = 1;
         g.p[0] = p;

@@ -269,12 +269,16 @@ struct BulkTuning {
     int rows_pair = 0;             // size each CTA to half an SM (see nm_rows.cuh)
     int rows_pre = 1;              // tasks per warp copied before the dependence wait (<= SW)
     int rows_l2pre_bytes = 0;      // weight bytes per CTA warmed in L2 before that wait
+    // tensor-core product (2:4, batch 8 and up; nm_spmm_tc.cu)
+    int tc = -1;                   // 1: wherever it applies, 0: never, -1: batch 8 with
+                                   // more than 128 rows a CTA (two MMA tiles)
+    int tc_lbo = 1;                // encoded leading-byte-offset field of its descriptors
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows (row-per-warp kernel), ctas, pdl
-// (both); read once per process.
+// (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 
 struct BulkPlan {

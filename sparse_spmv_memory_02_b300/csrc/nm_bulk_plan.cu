@@ -45,6 +45,8 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "rows_pair") && (v == 0 || v == 1)) t.rows_pair = v;
         else if (!std::strcmp(tok, "rows_pre") && v >= 0 && v <= 8) t.rows_pre = v;
         else if (!std::strcmp(tok, "rows_l2pre") && v >= 0) t.rows_l2pre_bytes = v;
+        else if (!std::strcmp(tok, "tc") && (v == -1 || v == 0 || v == 1)) t.tc = v;
+        else if (!std::strcmp(tok, "tc_lbo") && v >= 0 && v < 16384) t.tc_lbo = v;
     }
     return t;
 }
@@ -57,6 +59,13 @@ const BulkTuning &bulk_tuning()
 {
     static const BulkTuning t = parse_tuning();
     return t;
+}
+
+int spmm_tc_mode(uint32_t *lbo_enc)
+{
+    const BulkTuning &t = bulk_tuning();
+    *lbo_enc = static_cast<uint32_t>(t.tc_lbo);
+    return t.tc;
 }
 
 int max_dynamic_smem()

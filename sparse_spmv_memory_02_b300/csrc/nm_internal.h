@@ -80,6 +80,19 @@ cudaError_t launch_calib(const uint16_t *X, int64_t T, int64_t K, int64_t ldx, f
 uint32_t calib_idesc();
 uint64_t calib_desc_hi(uint32_t lbo, uint32_t sbo);
 
+// 2:4 product for batches of 8 to 32 on the tensor cores (nm_spmm_tc.cu):
+// applies to K % 128 == 0, ldx % 8 == 0, 16-byte aligned values, masks and
+// x, and at most 256 rows per CTA with one CTA per SM.  desc_hi: the
+// operands' shared-memory descriptor fields (spmm_tc_desc_hi(1)).
+bool spmm_tc_applies(const SpmvProblem &p, int nsm);
+cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s);
+uint32_t spmm_tc_idesc(int N);
+// When products take that path (tuning key tc: 1 wherever it applies, 0
+// never, -1 at batch 8 with more than 128 rows a CTA) and its descriptors'
+// encoded leading-byte-offset field (tuning key tc_lbo).
+int spmm_tc_mode(uint32_t *lbo_enc);
+uint64_t spmm_tc_desc_hi(uint32_t lbo_enc);
+
 // Cached device attributes of the current device.
 int sm_count();
 int max_dynamic_smem();

@@ -1,0 +1,553 @@
+// 2:4 sparse x dense product for batches of 8 to 32 vectors on the
+// fifth-generation tensor cores (tcgen05), for sm_103a.
+//
+// The same N:M product as the streaming kernels ("SparseDecoding:
+// Decoding-Aware Pruning for Accurate and Efficient LLM Inference",
+// Abstract: bitmask indexing, fixed-step traversal), for the regime where
+// the batch makes the CUDA-core kernel instruction-bound (8 x 8 products and
+// their x gathers per 16-byte chunk): the packed weights are still streamed
+// from HBM exactly once, but each CTA expands its rows to dense fp16 in
+// tensor memory and the tensor cores do the multiply.
+//
+//   * One CTA per SM, rows split evenly over the CTAs (at most 256 rows a
+//     CTA: two 128-row MMA tiles, the second possibly partial).
+//   * Warp 16 lane 0 streams 128-position slabs by TMA into a ring of up to
+//     16 stages: the CTA's rows' packed values (64 fp16 a row, 128-byte
+//     swizzled), their mask words (4 a row) and x (the batch rows, 128-byte
+//     swizzled, the MMA's B operand).
+//   * Warps 0-15 expand the slab: every 2:4 group's value pair goes to its
+//     two mask positions, zeros to the others (two byte permutes per group
+//     with selectors from a 16-entry table), and the dense row is stored into
+//     tensor memory (lane = row, two fp16 a column) as the MMA's A operand.
+//     Warp 4h + q serves lanes 32q..32q+31; with two tiles h / 2 picks the
+//     tile and h % 2 the half of the slab, with one tile h picks the quarter.
+//   * Warp 17 lane 0 issues tcgen05.mma (M = 128 per tile, N = the batch
+//     padded to 16 or 32, K = 16 positions, A from tensor memory, fp32
+//     accumulators in tensor memory) and commits once a slab.
+//   * Warps 0-15 read the accumulators (lane = row, column = vector) and
+//     round them into y.
+// Rows of a tile past the CTA's rows are never written: an MMA row depends
+// on its own A row only, and those accumulator rows are not stored.
+// Every mbarrier wait is bounded; a timeout sets the error word, the kernel
+// drains what it issued, releases its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "nm_device.cuh"
+#include "nm_internal.h"
+#include "nm_pipe.cuh"
+
+namespace nm {
+
+namespace {
+
+constexpr int kSlabPos = 128;        // K positions per slab
+constexpr int kMaxRows = 256;        // rows per CTA (two M tiles)
+constexpr int kTileM = 128;
+constexpr int kMaxStages = 16;
+constexpr int kMaxABufs = 7;         // A buffers in tensor memory
+constexpr int kExpWarps = 16;
+constexpr int kThreads = 32 * (kExpWarps + 2);
+constexpr uint32_t kTmemCols = 512;  // accumulators [0, 64), A buffers from 64
+constexpr uint32_t kAColBase = 64;
+
+// Wait without suspending the thread: the expanders and the MMA issuer hand
+// A buffers back and forth every slab, so a wake-up delay there is paid on
+// every slab.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_spin(uint64_t *bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(smem_addr(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+struct TcArgs {
+    void *y;
+    int64_t ldy;
+    int rows, K, batch, Np;   // Np: batch padded to a multiple of 16
+    int row_base, row_extra;  // CTA c owns row_base rows (+1 if c < row_extra)
+    int y_f32;
+    uint32_t idesc;
+    uint64_t desc_hi;         // K-major, 128-byte swizzle, SBO 1024
+    int box_rows;             // rows a values / masks box carries (max rows a CTA)
+    int S;                    // ring stages
+    int off_m, off_x;         // masks and x inside a stage
+    int stage_bytes, x_bytes, off_bar;
+    int x3d;                  // 1: x map is 3-D (one copy a slab), 0: 2-D (two copies)
+    unsigned int *err;
+};
+
+__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                      uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *map, int x, int y,
+                                      uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// D[tmem_d] (+)= A[tmem_a] * B[b_desc]: A in tensor memory, B in shared memory.
+__device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void commit_to(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+// 16 fp32 columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 16 32-bit columns into this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// Byte-permute selectors that expand a 2:4 group: for nibble n (the group's
+// mask bits), the two dense words (positions 0-1 and 2-3) of the group are
+// prmt(v, 0, sel & 0xFFFF) and prmt(v, 0, sel >> 16), v = the group's value
+// pair: each position takes v's low half (bytes 0-1), its high half (2-3)
+// or zero (bytes 4-5 of the zero operand).  Nibbles with other than two set
+// bits give zeros or unspecified picks (never an out-of-range byte).
+__host__ __device__ constexpr uint32_t expand_sel(uint32_t n)
+{
+    uint32_t s[4] = {0x54u, 0x54u, 0x54u, 0x54u};
+    int j = 0;
+    for (int q = 0; q < 4; ++q)
+        if ((n >> q) & 1u) {
+            if (j == 0) s[q] = 0x10u;
+            else if (j == 1) s[q] = 0x32u;
+            ++j;
+        }
+    return s[0] | (s[1] << 8) | (s[2] << 16) | (s[3] << 24);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
+                  const __grid_constant__ CUtensorMap tm_masks,
+                  const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TcArgs a)
+{
+    extern __shared__ uint8_t tc_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // [stage]: values | masks (off_m) | x (off_x); then barriers and the table
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.off_bar);
+    uint64_t *full = bars;                        // [S] TMA -> expanders, MMA
+    // done[j % Q]: the MMAs of slab j have completed (one commit a slab).
+    // That frees slab j's stage for the producer and its A buffer for the
+    // expanders: the MMAs were issued only after every expander had read
+    // the stage.  Q exceeds both ring depths, so no waiter can miss a phase.
+    uint64_t *done = full + kMaxStages;           // [Q] MMA -> producer, expanders
+    uint64_t *afull = done + kMaxStages + 1;      // [nbuf] expanders -> MMA
+    uint64_t *acc = afull + kMaxABufs;            // MMA -> epilogue
+    uint2 *sel_tab = reinterpret_cast<uint2 *>(acc + 1);  // [16]: both words' selectors
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sel_tab + 16);
+    volatile int *failed = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int r_begin = cta * a.row_base + min(cta, a.row_extra);
+    const int r_count = a.row_base + (cta < a.row_extra ? 1 : 0);
+    const int ntile = (r_count + kTileM - 1) / kTileM;  // 1 or 2
+    const int nslab = a.K / kSlabPos;
+    const int S = a.S;
+    // A buffers: ntile x 64 columns each after the accumulators' 64
+    const uint32_t buf_cols = static_cast<uint32_t>(ntile) * 64u;
+    const int nbuf = min(kMaxABufs, static_cast<int>((kTmemCols - kAColBase) / buf_cols));
+    const int Q = max(S, nbuf) + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        for (int j = 0; j < Q; ++j) mbar_init(&done[j], 1);
+        for (int d = 0; d < nbuf; ++d) mbar_init(&afull[d], kExpWarps);  // one arrive a warp
+        mbar_init(acc, 1);
+        *failed = 0;
+        mbar_fence_init();
+    }
+    if (threadIdx.x < 16) {
+        const uint32_t sel = expand_sel(threadIdx.x);
+        sel_tab[threadIdx.x] = make_uint2(sel & 0xFFFFu, sel >> 16);
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kExpWarps) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_map(&tm_vals);
+            prefetch_map(&tm_masks);
+            prefetch_map(&tm_x);
+            const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x);
+            int issued = 0;
+            for (int k = 0; k < nslab && !*failed; ++k) {
+                const int s = k % S;
+                if (k >= S && !mbar_wait(&done[(k - S) % Q], ((k - S) / Q) & 1)) {
+                    *failed = 1;
+                    atomicOr(a.err, kDevErrPipeTimeout);
+                    break;
+                }
+                uint8_t *st = smem + s * a.stage_bytes;
+                // CTAs start at different slabs (the sum is order-free), so
+                // they do not all read the same x lines at the same moment
+                int ks = k + slab0;
+                if (ks >= nslab) ks -= nslab;
+                // a box always lands whole (rows past the matrix read as zeros)
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(
+                                                    a.box_rows * (128 + 16) + a.x_bytes));
+                tma2d(st, &tm_vals, ks * 64, r_begin, &full[s]);
+                tma2d(st + a.off_m, &tm_masks, ks * 4, r_begin, &full[s]);
+                // x: both 64-position boxes of the slab
+                if (a.x3d) {
+                    tma3d(st + a.off_x, &tm_x, 0, 0, 2 * ks, &full[s]);
+                } else {
+                    tma2d(st + a.off_x, &tm_x, ks * kSlabPos, 0, &full[s]);
+                    tma2d(st + a.off_x + a.x_bytes / 2, &tm_x, ks * kSlabPos + 64, 0, &full[s]);
+                }
+                ++issued;
+            }
+            for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
+                if (!mbar_wait(&full[k % S], (k / S) & 1)) break;
+        }
+    } else if (warp == kExpWarps + 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            for (int k = 0; k < nslab; ++k) {
+                const int s = k % S, d = k % nbuf;
+                if (*failed) break;
+                if (!mbar_spin(&full[s], (k / S) & 1) || !mbar_spin(&afull[d], (k / nbuf) & 1)) {
+                    *failed = 1;
+                    atomicOr(a.err, kDevErrPipeTimeout);
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t xb = smem_addr(smem + s * a.stage_bytes + a.off_x);
+                for (int t = 0; t < ntile; ++t) {
+                    const uint32_t ta = tmem + kAColBase + d * buf_cols + t * 64;
+#pragma unroll
+                    for (int kk = 0; kk < kSlabPos / 16; ++kk) {
+                        // x: 64-position box kk / 4, 32-byte step kk % 4 inside it
+                        const uint32_t boff = (kk >> 2) * (a.x_bytes / 2) + (kk & 3) * 32;
+                        mma_ts(tmem + t * a.Np, ta + kk * 8, a.desc_hi | ((xb + boff) >> 4),
+                               a.idesc, (k | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                commit_to(&done[k % Q]);
+            }
+            commit_to(acc);
+        }
+    } else {
+        // ------------------------------------------------ expanders (warps 0-15)
+        const int q = warp & 3;
+        // warp = 4 h + q: lanes 32q.. of a tile; with two tiles, h / 2 is
+        // the tile and h % 2 the half of the slab, with one, h the quarter
+        const int h = warp >> 2;
+        const int tile = ntile == 2 ? (h >> 1) : 0;
+        const int c_lo = ntile == 2 ? 8 * (h & 1) : 4 * h;
+        const int nc4 = ntile == 2 ? 2 : 1;            // groups of 4 chunks
+        const int rr = tile * kTileM + 32 * q + lane;  // row of this lane in the CTA
+        const bool warp_live = tile * kTileM + 32 * q < r_count;
+        const int rs = rr < r_count ? rr : 0;          // lanes past the rows read row 0
+        for (int k = 0; k < nslab; ++k) {
+            const int s = k % S, d = k % nbuf;
+            // lane 0 polls for the warp
+            int ok = 0;
+            if (lane == 0)
+                ok = !*failed && mbar_spin(&full[s], (k / S) & 1) &&
+                     (k < nbuf || mbar_spin(&done[(k - nbuf) % Q], ((k - nbuf) / Q) & 1));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            __syncwarp();
+            if (!ok) {
+                if (lane == 0 && !*failed) {
+                    *failed = 1;
+                    atomicOr(a.err, kDevErrPipeTimeout);
+                }
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (warp_live) {
+                const uint8_t *st = smem + s * a.stage_bytes;
+                // the values box lands 128-byte swizzled: 16-byte chunk j of
+                // row r at r * 128 + ((j ^ (r % 8)) * 16)
+                const uint8_t *vrow = st + rs * 128;
+                const uint4 m4 = *reinterpret_cast<const uint4 *>(st + a.off_m + rs * 16);
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAColBase +
+                                    d * buf_cols + tile * 64 + c_lo * 4;
+                for (int g4 = 0; g4 < nc4; ++g4) {
+                    // four chunks = 32 positions = one mask word
+                    const int g = (c_lo >> 2) + g4;
+                    const uint32_t mword = g == 0 ? m4.x : g == 1 ? m4.y : g == 2 ? m4.z : m4.w;
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        // dense chunk c: positions 8c .. 8c+7 = groups 2c, 2c+1
+                        // (value words 2c and 2c+1 of the row)
+                        const int c = c_lo + 4 * g4 + j;
+                        const uint4 vv = *reinterpret_cast<const uint4 *>(
+                            vrow + (((c >> 1) ^ (rs & 7)) << 4));
+                        const uint32_t v0 = (c & 1) ? vv.z : vv.x;
+                        const uint32_t v1 = (c & 1) ? vv.w : vv.y;
+                        const uint32_t bits = mword >> (8 * j);
+                        const uint2 s0 = sel_tab[bits & 15u], s1 = sel_tab[(bits >> 4) & 15u];
+                        w[4 * j + 0] = prmt(v0, 0u, s0.x);
+                        w[4 * j + 1] = prmt(v0, 0u, s0.y);
+                        w[4 * j + 2] = prmt(v1, 0u, s1.x);
+                        w[4 * j + 3] = prmt(v1, 0u, s1.y);
+                    }
+                    tmem_st16(ta + 16 * g4, w);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[d]);
+        }
+    }
+
+    // ---------------------------------------------------- epilogue
+    __syncwarp();
+    bool ok = true;
+    if (warp < kExpWarps) ok = __all_sync(0xffffffffu, mbar_wait(acc, 0)) != 0;
+    if (!ok && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
+    const bool go = __syncthreads_and(ok && *failed == 0) != 0;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // warp = 4 h + q reads lanes 32q.. of tile h / 2 (two tiles) or 0, from
+    // column 16 * (h % 2) or 16 * h in steps of 32 or 64
+    const int eh = warp >> 2;
+    const int b_lo = ntile == 2 ? 16 * (eh & 1) : 16 * eh;
+    if (go && warp < kExpWarps && b_lo < a.Np) {
+        const int q = warp & 3;
+        const int tile = ntile == 2 ? (eh >> 1) : 0;
+        const int b_step = ntile == 2 ? 32 : 64;
+        const int row = tile * kTileM + 32 * q + lane;
+        for (int b0 = b_lo; b0 < a.Np; b0 += b_step) {
+            float v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + tile * a.Np + b0, v);
+            if (row < r_count) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (b0 + j < a.batch)
+                        store_y(a.y, (b0 + j) * a.ldy + r_begin + row, v[j], a.y_f32 != 0);
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled_tc()
+{
+    static std::once_flag once;
+    static EncodeTiled fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// x [batch][ldx] fp16 viewed as {64 positions, batch rows, K/64 blocks}: a
+// {64, Np, 2} box lands as two [Np][64] boxes (the slab's positions 0-63,
+// then 64-127), 128-byte swizzled.
+bool encode_x3d(EncodeTiled enc, CUtensorMap *m, const void *x, uint64_t K, uint64_t batch,
+                uint64_t ldx_bytes, uint32_t Np)
+{
+    const cuuint64_t dims[3] = {64, batch, K / 64};
+    const cuuint64_t strides[2] = {ldx_bytes, 128};
+    const cuuint32_t box[3] = {64, Np, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(x), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode2d(EncodeTiled enc, CUtensorMap *m, CUtensorMapDataType dt, const void *base,
+              uint64_t inner, uint64_t outer, uint64_t stride_bytes, uint32_t box_inner,
+              uint32_t box_outer, CUtensorMapSwizzle sw)
+{
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// tcgen05 kind::f16 instruction descriptor: fp32 accumulator, fp16 A and B,
+// both K-major, N / 8 at bit 17, M / 16 at bit 24.
+uint32_t spmm_tc_idesc(int N) { return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (8u << 24); }
+
+// K-major operand, 128-byte swizzle: 8-row groups 1024 bytes apart (SBO),
+// LBO unused by this layout (encoded lbo), version 1, layout 2.
+uint64_t spmm_tc_desc_hi(uint32_t lbo_enc)
+{
+    return (static_cast<uint64_t>(lbo_enc & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+bool spmm_tc_applies(const SpmvProblem &p, int nsm)
+{
+    if (p.N != 2 || p.M != 4 || p.batch < 8 || p.batch > 32) return false;
+    if (p.K % kSlabPos != 0 || p.K / 2 > (1ll << 31) || p.rows < 1) return false;
+    if (p.ldx % 8 != 0) return false;
+    // tensor-map bases must be 16-byte aligned
+    if ((reinterpret_cast<uintptr_t>(p.values) | reinterpret_cast<uintptr_t>(p.masks) |
+         reinterpret_cast<uintptr_t>(p.x)) & 15u)
+        return false;
+    const int64_t grid = std::min<int64_t>(p.rows, nsm);
+    return (p.rows + grid - 1) / grid <= kMaxRows;
+}
+
+cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s)
+{
+    EncodeTiled enc = encode_tiled_tc();
+    if (!enc) return cudaErrorNotSupported;
+    const int nsm = sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
+    const int Np = p.batch <= 16 ? 16 : 32;
+    const int64_t Lv = p.K / 2;          // fp16 values a row
+    const int64_t Lm = p.K / 32;         // mask words a row
+    const int grid = static_cast<int>(std::min<int64_t>(p.rows, nsm));
+    const int box_rows = static_cast<int>(p.rows / grid + (p.rows % grid ? 1 : 0));
+    if (box_rows > kMaxRows) return cudaErrorNotSupported;
+    CUtensorMap tv, tm, tx;
+    if (!encode2d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.values, Lv, p.rows, Lv * 2, 64,
+                  box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode2d(enc, &tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, p.masks, Lm, p.rows, Lm * 4, 4,
+                  box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorNotSupported;  // the caller takes another kernel
+    // the 3-D view of x has a stride (128 bytes) below the row pitch; a
+    // driver that refuses it gets the 2-D map and two copies a slab
+    int x3d = 1;
+    if (!encode_x3d(enc, &tx, p.x, p.K, p.batch, p.ldx * 2, Np)) {
+        x3d = 0;
+        if (!encode2d(enc, &tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.batch, p.ldx * 2, 64,
+                      Np, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorNotSupported;  // the caller takes another kernel
+    }
+    TcArgs a = {};
+    a.x3d = x3d;
+    a.box_rows = box_rows;
+    a.y = p.y;
+    a.ldy = p.ldy;
+    a.rows = static_cast<int>(p.rows);
+    a.K = static_cast<int>(p.K);
+    a.batch = p.batch;
+    a.Np = Np;
+    a.row_base = static_cast<int>(p.rows / grid);
+    a.row_extra = static_cast<int>(p.rows % grid);
+    a.y_f32 = p.y_f32 ? 1 : 0;
+    a.idesc = spmm_tc_idesc(Np);
+    a.desc_hi = desc_hi;
+    a.x_bytes = 2 * Np * 128;  // two 64-position boxes of Np rows
+    a.off_m = (box_rows * 128 + 1023) / 1024 * 1024;
+    a.off_x = a.off_m + (box_rows * 16 + 1023) / 1024 * 1024;
+    a.stage_bytes = a.off_x + a.x_bytes;
+    const int tail = 1024 + 512;  // alignment slack, barriers and table
+    const int avail = max_dynamic_smem();
+    if (avail <= 0) return cudaErrorInvalidDevice;
+    a.S = std::min(kMaxStages, (avail - tail) / a.stage_bytes);
+    if (a.S < 2) return cudaErrorNotSupported;
+    a.off_bar = a.S * a.stage_bytes;
+    a.err = p.err;
+    const int smem = a.off_bar + tail;
+    static std::atomic<int> smem_set{0};
+    if (smem > smem_set.load(std::memory_order_relaxed)) {
+        cudaError_t e =
+            cudaFuncSetAttribute(nm_spmm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set.store(smem, std::memory_order_relaxed);
+    }
+    nm_spmm_tc_kernel<<<grid, kThreads, smem, s>>>(tv, tm, tx, a);
+    return cudaGetLastError();
+}
+
+}  // namespace nm

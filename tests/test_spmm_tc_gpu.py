@@ -1,0 +1,110 @@
+"""GPU parity of the tensor-core 2:4 product (tcgen05, A operand expanded
+into tensor memory) against the CPU oracle.
+
+The path is taken by default for 2:4 products at batch 8 on layers with more
+than 128 rows per SM; the forced tuning ``tc=1`` (read once per process, so
+run in a child) makes every 2:4 product with K a multiple of 128 and at most
+256 rows per CTA take it.  Shapes cover one row, fewer rows than SMs, ragged
+row splits, one and two 128-row MMA tiles (the second partial), the largest
+split that still fits (256 rows per CTA), splits just past it and K not a
+multiple of 128 (both fall back to the CUDA-core kernels), fp16 and fp32 y,
+and x and y with row strides wider than the matrix.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import nm_synth
+import oracle
+from sparse_spmv_memory_02_b300 import nm
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+_CHILD = r"""
+import json, sys
+import numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import nm_synth, oracle
+from sparse_spmv_memory_02_b300 import nm
+g = np.random.default_rng(1)
+nsm = torch.cuda.get_device_properties(0).multi_processor_count
+fails = []
+for (rows, K, B, wide, f32) in json.loads(sys.argv[2]):
+    rows = rows if rows > 0 else -rows * nsm     # negative: rows per SM
+    W = nm_synth.weights(rows, K, rows + K, "cuda")
+    mask = nm_synth.topn_mask(W, 2, 4)
+    A = nm.nm_pack(W, mask, 2, 4)
+    xs = nm_synth.activations(K + (64 if wide else 0), B, rows + 3, True, "cuda")
+    x = xs[:, :K]
+    ydt = torch.float32 if f32 else torch.float16
+    ybuf = torch.full((B, rows + (40 if wide else 0)), float("nan"), dtype=ydt, device="cuda")
+    y = ybuf[:, :rows]
+    nm.nm_spmv_batched(A, x, y)
+    torch.cuda.synchronize()
+    if wide and not torch.isnan(ybuf[:, rows:].float()).all():
+        fails.append([rows, K, B, "wrote past ldy"])
+    pick = np.arange(rows) if rows <= 1024 else np.sort(g.choice(rows, 512, replace=False))
+    idx = torch.from_numpy(pick).to("cuda")
+    Wn = W[idx].cpu().numpy().view(np.uint16)
+    xn = x.contiguous().cpu().numpy().view(np.uint16)
+    yr, sr = oracle.spmv_dense(Wn, mask[idx].cpu().numpy(), xn)
+    yg = y[:, idx].double().cpu().numpy()
+    ok = oracle.within_tolerance(yg, yr, sr)
+    if not ok.all():
+        fails.append([rows, K, B, int((~ok).sum())])
+print(json.dumps({"fails": fails, "errors": nm.nm_device_errors()}))
+"""
+
+# (rows, K, batch, wide strides, fp32 y); rows < 0 means -rows per SM
+CASES = [
+    (1, 128, 8, False, True),
+    (149, 1024, 8, True, True),
+    (300, 256, 8, False, False),
+    (4096, 4096, 8, True, True),
+    (28672, 512, 8, False, True),     # two tiles, the second partial
+    (-256, 384, 8, False, True),      # 256 rows a CTA: both tiles full
+    (-257, 256, 8, False, True),      # 257 rows a CTA: CUDA-core kernels
+    (37000, 384, 8, True, False),
+    (3000, 4000, 8, False, True),     # K not a multiple of 128
+    (5000, 2048, 5, False, True),     # batch below 8: CUDA-core kernels
+]
+
+
+def test_tensor_core_path_forced():
+    env = dict(os.environ, NM_BULK_TUNE="tc=1")
+    r = subprocess.run([sys.executable, "-c", _CHILD, ROOT, json.dumps(CASES)], env=env,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    assert out["fails"] == [] and out["errors"] == 0, out
+
+
+def test_tensor_core_path_default_on_70b_gate_batch8():
+    """The gate projection of the 70B-shaped block (28672 x 8192) at batch 8
+    takes the tensor-core path by default: sampled rows against the oracle,
+    and a repeated call gives the same bits."""
+    rows, K, B = 28672, 8192, 8
+    W = nm_synth.weights(rows, K, 77, DEV)
+    mask = nm_synth.topn_mask(W, 2, 4)
+    A = nm.nm_pack(W, mask, 2, 4)
+    x = nm_synth.activations(K, B, 78, True, DEV)
+    y = nm.nm_spmv_batched(A, x, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(3)
+    pick = np.sort(g.choice(rows, 384, replace=False))
+    idx = torch.from_numpy(pick).to(DEV)
+    yr, sr = oracle.spmv_dense(W[idx].cpu().numpy().view(np.uint16), mask[idx].cpu().numpy(),
+                               x.cpu().numpy().view(np.uint16))
+    ok = oracle.within_tolerance(y[:, idx].double().cpu().numpy(), yr, sr)
+    assert ok.all(), "%d/%d outside tolerance" % ((~ok).sum(), ok.size)
+    assert nm.nm_device_errors() == 0
+    y2 = nm.nm_spmv_batched(A, x, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
