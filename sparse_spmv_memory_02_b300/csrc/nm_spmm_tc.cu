@@ -21,9 +21,10 @@
 //     tensor memory (lane = row, two fp16 a column) as the MMA's A operand.
 //     Warp 4h + q serves lanes 32q..32q+31; with two tiles h / 2 picks the
 //     tile and h % 2 the half of the slab, with one tile h picks the quarter.
-//   * Warp 17 lane 0 issues tcgen05.mma (M = 128 per tile, N = the batch
-//     padded to 16 or 32, K = 16 positions, A from tensor memory, fp32
-//     accumulators in tensor memory) and commits once a slab.
+//   * Warps 17-20 (lane 0) issue tcgen05.mma (M = 128 per tile, N = the
+//     batch padded to 16 or 32, K = 16 positions, A from tensor memory, fp32
+//     accumulators in tensor memory), each a quarter of the slab's MMAs into
+//     its own accumulator, and commit once a slab.
 //   * Warps 0-15 read the accumulators (lane = row, column = vector) and
 //     round them into y.
 // Rows of a tile past the CTA's rows are never written: an MMA row depends
@@ -52,9 +53,10 @@ constexpr int kTileM = 128;
 constexpr int kMaxStages = 16;
 constexpr int kMaxABufs = 7;         // A buffers in tensor memory
 constexpr int kExpWarps = 16;
-constexpr int kThreads = 32 * (kExpWarps + 2);
-constexpr uint32_t kTmemCols = 512;  // accumulators [0, 64), A buffers from 64
-constexpr uint32_t kAColBase = 64;
+constexpr int kMmaWarps = 4;         // MMA issuers, each with its own accumulator
+constexpr int kThreads = 32 * (kExpWarps + 1 + kMmaWarps);
+constexpr uint32_t kTmemCols = 512;  // accumulators [0, 4 Np <= 128), A buffers from 128
+constexpr uint32_t kAColBase = 128;
 
 // Wait without suspending the thread: the expanders and the MMA issuer hand
 // A buffers back and forth every slab, so a wake-up delay there is paid on
@@ -220,9 +222,9 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-        for (int j = 0; j < Q; ++j) mbar_init(&done[j], 1);
+        for (int j = 0; j < Q; ++j) mbar_init(&done[j], kMmaWarps);  // one commit an issuer
         for (int d = 0; d < nbuf; ++d) mbar_init(&afull[d], kExpWarps);  // one arrive a warp
-        mbar_init(acc, 1);
+        mbar_init(acc, kMmaWarps);
         *failed = 0;
         mbar_fence_init();
     }
@@ -279,8 +281,19 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
             for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
                 if (!mbar_wait(&full[k % S], (k / S) & 1)) break;
         }
-    } else if (warp == kExpWarps + 1) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp > kExpWarps) {
+        // ------------------------------------------------ MMA issuers
+        // A thread waits ~120 cycles on each tcgen05.mma it issues, whatever
+        // N is, while several issuing threads proceed in parallel, so four
+        // issuers split a slab: with two tiles issuer i takes tile i / 2 and
+        // K steps 4 (i % 2) .. +3, with one tile K steps 2i, 2i + 1.  Each
+        // accumulates into its own columns (i * Np); the epilogue adds the
+        // partial sums.
+        const int mi = warp - kExpWarps - 1;
+        const int t = ntile == 2 ? (mi >> 1) : 0;
+        const int kk0 = ntile == 2 ? 4 * (mi & 1) : 2 * mi;
+        const int nkk = ntile == 2 ? 4 : 2;
+        const uint32_t dcol = tmem + static_cast<uint32_t>(mi * a.Np);
         if (lane == 0) {
             for (int k = 0; k < nslab; ++k) {
                 const int s = k % S, d = k % nbuf;
@@ -292,15 +305,12 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t xb = smem_addr(smem + s * a.stage_bytes + a.off_x);
-                for (int t = 0; t < ntile; ++t) {
-                    const uint32_t ta = tmem + kAColBase + d * buf_cols + t * 64;
-#pragma unroll
-                    for (int kk = 0; kk < kSlabPos / 16; ++kk) {
-                        // x: 64-position box kk / 4, 32-byte step kk % 4 inside it
-                        const uint32_t boff = (kk >> 2) * (a.x_bytes / 2) + (kk & 3) * 32;
-                        mma_ts(tmem + t * a.Np, ta + kk * 8, a.desc_hi | ((xb + boff) >> 4),
-                               a.idesc, (k | kk) != 0 ? 1u : 0u);
-                    }
+                const uint32_t ta = tmem + kAColBase + d * buf_cols + t * 64;
+                for (int kk = kk0; kk < kk0 + nkk; ++kk) {
+                    // x: 64-position box kk / 4, 32-byte step kk % 4 inside it
+                    const uint32_t boff = (kk >> 2) * (a.x_bytes / 2) + (kk & 3) * 32;
+                    mma_ts(dcol, ta + kk * 8, a.desc_hi | ((xb + boff) >> 4), a.idesc,
+                           (k > 0 || kk > kk0) ? 1u : 0u);
                 }
                 commit_to(&done[k % Q]);
             }
@@ -390,9 +400,19 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
         const int tile = ntile == 2 ? (eh >> 1) : 0;
         const int b_step = ntile == 2 ? 32 : 64;
         const int row = tile * kTileM + 32 * q + lane;
+        // the tile's partial sums: issuers 2 tile, 2 tile + 1 (two tiles) or 0-3
+        const int p0 = ntile == 2 ? 2 * tile : 0;
+        const int np = ntile == 2 ? 2 : 4;
         for (int b0 = b_lo; b0 < a.Np; b0 += b_step) {
             float v[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + tile * a.Np + b0, v);
+            const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
+            tmem_ld16(tmem + lanes + p0 * a.Np + b0, v);
+            for (int pi = 1; pi < np; ++pi) {
+                float w[16];
+                tmem_ld16(tmem + lanes + (p0 + pi) * a.Np + b0, w);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += w[j];
+            }
             if (row < r_count) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
