@@ -286,11 +286,15 @@ nm_status nm_spmv_gate_up_silu(const nm_matrix *gate, const nm_matrix *up, const
  * waits (shared-memory barriers between its copy and compute warps) has not
  * completed within about two seconds; the kernel then stops waiting, ends,
  * and the y it wrote is unspecified.  This never happens in a correct run;
- * the word lets a caller check for it after the fact.  Synchronises
- * `stream` (so it cannot be captured in a CUDA graph).
+ * the word lets a caller check for it after the fact.  The tensor-core
+ * product sets NM_DEVERR_SMEM_ALIGN, and writes nothing, if its dynamic
+ * shared memory does not start on a 1024-byte boundary (its swizzled copies
+ * need that; CUDA places it there).  Synchronises `stream` (so it cannot be
+ * captured in a CUDA graph).
  * Errors: NM_ERR_INVALID_ARG (flags NULL, capturing stream), NM_ERR_CUDA.
  */
 #define NM_DEVERR_PIPE_TIMEOUT 1u
+#define NM_DEVERR_SMEM_ALIGN 2u
 nm_status nm_device_errors(uint32_t *flags, int clear, nm_stream_t stream);
 
 /* Static, human-readable name of a status code. */

@@ -12,6 +12,7 @@ namespace nm {
 
 // Bits of the library's device error word (read back by nm_device_errors).
 constexpr unsigned int kDevErrPipeTimeout = 1u;  // an mbarrier wait hit its time limit
+constexpr unsigned int kDevErrSmemAlign = 2u;    // dynamic shared memory not 1024-byte aligned
 
 // A wait that has not completed after this many nanoseconds is abandoned.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -193,9 +193,16 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
                   const __grid_constant__ CUtensorMap tm_masks,
                   const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TcArgs a)
 {
-    extern __shared__ uint8_t tc_smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // Used as declared (not re-aligned through an integer), so every pointer
+    // below stays visibly in shared memory and the compiler emits shared-
+    // space loads.  The 128-byte-swizzled copies need the 1024-byte
+    // alignment: checked, and the kernel does nothing without it.
+    extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
+    uint8_t *smem = tc_smem_raw;
+    if (smem_addr(tc_smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(a.err, kDevErrSmemAlign);
+        return;
+    }
     // [stage]: values | masks (off_m) | x (off_x); then barriers and the table
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.off_bar);
     uint64_t *full = bars;                        // [S] TMA -> expanders, MMA

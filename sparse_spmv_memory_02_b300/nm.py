@@ -107,6 +107,7 @@ def nm_version() -> int:
 
 
 NM_DEVERR_PIPE_TIMEOUT = 1
+NM_DEVERR_SMEM_ALIGN = 2
 
 
 def nm_device_errors(clear: bool = True, stream=None) -> int:
