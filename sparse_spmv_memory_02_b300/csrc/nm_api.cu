@@ -229,16 +229,22 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
 // One product on the best kernel that applies: the row kernel (any batch;
 // K a multiple of 128), the chunk-column kernel (when no row plan fits in
 // shared memory), the direct-load kernel, the scalar kernel.
+// 2:4 at batch 8 on layers with more than 128 rows an SM: the tensor-core
+// product (the CUDA-core kernel is instruction-bound there).  Tuning key tc
+// forces it on (1) or off (0).
+bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
+{
+    const int tc = nm::spmm_tc_mode(lbo_enc);
+    const int nsm = nm::sm_count();
+    return tc != 0 && nm::spmm_tc_applies(p, nsm) &&
+           (tc == 1 || (p.batch == 8 && p.rows > 128LL * nsm));
+}
+
 nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)
 {
     cudaError_t e = cudaErrorNotSupported;
-    // 2:4 at batch 8 on layers with more than 128 rows an SM: the tensor-core
-    // product (the CUDA-core kernel is instruction-bound there)
     uint32_t tc_lbo = 0;
-    const int tc = nm::spmm_tc_mode(&tc_lbo);
-    const int nsm = nm::sm_count();
-    if (tc != 0 && nm::spmm_tc_applies(p, nsm) &&
-        (tc == 1 || (p.batch == 8 && p.rows > 128LL * nsm)))
+    if (takes_tensor_cores(p, &tc_lbo))
         e = nm::launch_spmm_tc(p, nm::spmm_tc_desc_hi(tc_lbo), s);
     if (e == cudaErrorNotSupported && nm::bulk_path_applies(p.N, p.M, p.K)) {
         nm::SpmvGroup g;
@@ -494,9 +500,18 @@ nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int
         }
         ++g.count;
     }
+    // members that all take the tensor-core product (the 70B-shaped gate/up
+    // at batch 8) run as separate launches of it, faster than one fused
+    // CUDA-core launch
+    bool all_tc = g.count > 0;
+    for (int i = 0; i < g.count && all_tc; ++i) {
+        uint32_t lbo = 0;
+        all_tc = takes_tensor_cores(g.p[i], &lbo);
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
-    if (fusable && g.count > 1 && nm::bulk_path_applies(g.p[0].N, g.p[0].M, g.p[0].K))
+    if (fusable && !all_tc && g.count > 1 &&
+        nm::bulk_path_applies(g.p[0].N, g.p[0].M, g.p[0].K))
         e = nm::launch_rows(g, s);
     if (e == cudaSuccess) return NM_OK;
     if (e != cudaErrorNotSupported) return cuda_fail(e, "nm_spmv_group launch");
