@@ -236,3 +236,21 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(nm, "_lib", None)
     with pytest.raises(ImportError):
         nm.lib()
+
+
+def test_binding_constants_match_the_header():
+    """Every integer #define of include/nm.h that the Python binding mirrors
+    (batch and group limits, device error bits, ...) has the same value, and
+    the enums' values are those of the binding's names."""
+    text = open(HEADER).read()
+    defines = {k: int(v.rstrip("uUlL"), 0)
+               for k, v in re.findall(r"#define (NM_\w+) (0x[0-9a-fA-F]+|\d+)[uUlL]*", text)}
+    mirrored = [k for k in defines if hasattr(nm, k)]
+    assert {"NM_MAX_BATCH", "NM_MAX_GROUP", "NM_DEVERR_PIPE_TIMEOUT",
+            "NM_DEVERR_SMEM_ALIGN"} <= set(mirrored), mirrored
+    for k in mirrored:
+        assert getattr(nm, k) == defines[k], k
+    enums = dict(re.findall(r"\b(NM_(?:OK|ERR_\w+|F16|F32))\s*=\s*(\d+)", text))
+    assert len(enums) == 7, enums
+    for k, v in enums.items():
+        assert getattr(nm, k) == int(v), k
