@@ -174,7 +174,14 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
  *   x  fp16 [batch][ldx], device; ldx >= K; with batch > 1, ldx must be a
  *      multiple of 8 so that every vector starts 16-byte aligned.
  *   y  y_type [batch][ldy], device; ldy >= rows.  Row b of y receives A x_b.
- * Same semantics and errors as nm_spmv.
+ * Same semantics and errors as nm_spmv.  At batch 8, a 2:4 matrix with more
+ * than 128 rows per SM (K a multiple of 128, at most 256 rows per SM, x and
+ * the packed arrays 16-byte aligned) is multiplied on the tensor cores: its
+ * groups are expanded to dense fp16 on chip and multiplied with fp32
+ * accumulation in another order, within the same error bound and
+ * deterministic from call to call; it does not use programmatic dependent
+ * launch.  NM_BULK_TUNE=tc=0 turns this off, tc=1 takes it for every 2:4
+ * product at batch 8 that it can run.
  */
 nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
                           void *y, int64_t ldy, int batch, nm_dtype y_type,
@@ -195,8 +202,9 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
  *   batch, ldx, y_type, stream: as nm_spmv_batched, shared by all products.
  * Each product's arguments are checked as by nm_spmv_batched (errors name
  * the matrix); matrices that differ in N, M or K are NM_ERR_INVALID_ARG.
- * When the shapes cannot share a launch the products are launched one by
- * one, with the same results.  Asynchronous, allocates nothing, may be
+ * When the shapes cannot share a launch, or every product takes the
+ * tensor-core path of nm_spmv_batched, the products are launched one by one,
+ * with the same results.  Asynchronous, allocates nothing, may be
  * captured in a CUDA graph; the products' y must not overlap.
  */
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
