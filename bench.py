@@ -487,13 +487,27 @@ def _eager_time(run, n, warmup=3):
     return statistics.median(times)
 
 
+def _libnm_kernel(rows, batch):
+    """Which kernel libnm runs for a 2:4 product with K a multiple of 128
+    (the library's routing rule, restated for the report; NM_BULK_TUNE tc=0/1
+    overrides it there and here)."""
+    tune = dict(kv.split("=", 1) for kv in os.environ.get("NM_BULK_TUNE", "").split(",")
+                if "=" in kv)
+    tc = int(tune.get("tc", "-1"))
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    fits = batch == 8 and (rows + nsm - 1) // nsm <= 256
+    if tc != 0 and fits and (tc == 1 or rows > 128 * nsm):
+        return "tensor-core 2:4 product (tcgen05)"
+    return "CUDA-core row kernel"
+
+
 def crossover_pass(batches=(1, 2, 4, 8, 16, 32, 64)):
     """The batch at which a 2:4 sparse-tensor-core GEMM (cuSPARSELt through
     torch's semi-structured sparse tensors, a library comparator) overtakes
-    this library's bandwidth kernel, on the Llama-3.3-70B-shaped gate layer
-    (28672 x 8192, 2:4): microseconds per product for libnm (batch <= 8),
-    the sparse tensor cores and dense cuBLAS on the masked weights, all
-    launched eagerly."""
+    this library, on the Llama-3.3-70B-shaped gate layer (28672 x 8192, 2:4):
+    microseconds per product for libnm (batch <= 8; the CUDA-core row kernel,
+    or at batch 8 the library's tensor-core 2:4 product), the sparse tensor
+    cores and dense cuBLAS on the masked weights, all launched eagerly."""
     from sparse_spmv_memory_02_b300 import nm
     rows, K = 28672, 8192
     W = nm_synth.weights(rows, K, 4242, "cuda")
@@ -514,6 +528,10 @@ def crossover_pass(batches=(1, 2, 4, 8, 16, 32, 64)):
         Xt = X.t().contiguous()
         row = {"batch": B}
         if B <= nm.NM_MAX_BATCH:
+            try:
+                row["libnm_kernel"] = _libnm_kernel(rows, B)
+            except Exception as e:  # a label only: never costs the timing
+                row["libnm_kernel"] = "unknown (%s)" % type(e).__name__
             y = torch.empty(B, rows, dtype=torch.float16, device="cuda")
 
             def ours():
