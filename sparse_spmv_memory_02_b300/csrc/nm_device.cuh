@@ -59,17 +59,32 @@ __device__ __forceinline__ uint4 ld_keep_v4(const uint4 *p)
 
 // ---------------------------------------------------------------- bits
 // Byte permute: result byte i = byte (sel >> 4i) & 7 of the 8-byte {hi, lo}.
-__device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
+// The bit helpers below also compile for the host (the same results, so the
+// mask decode can be checked on a machine without a GPU).
+__host__ __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
 {
+#ifdef __CUDA_ARCH__
     return __byte_perm(lo, hi, sel);
+#else
+    const uint64_t b = (static_cast<uint64_t>(hi) << 32) | lo;
+    uint32_t r = 0;
+    for (int i = 0; i < 4; ++i)
+        r |= static_cast<uint32_t>((b >> (8 * ((sel >> (4 * i)) & 7u))) & 0xFFu) << (8 * i);
+    return r;
+#endif
 }
 
+#ifdef __CUDA_ARCH__
 __device__ __forceinline__ uint32_t ctz(uint32_t v) { return __ffs(v) - 1; }   // v != 0
 __device__ __forceinline__ uint32_t msb(uint32_t v) { return 31 - __clz(v); }  // v != 0
+#else
+inline uint32_t ctz(uint32_t v) { return static_cast<uint32_t>(__builtin_ctz(v)); }
+inline uint32_t msb(uint32_t v) { return 31u - static_cast<uint32_t>(__builtin_clz(v)); }
+#endif
 
 // Selector that gathers fp16 lanes pa and pb (0..3) of the 8-byte pair
 // {hi, lo} into the low and high half of a 32-bit word.
-__device__ __forceinline__ uint32_t sel_pair(uint32_t pa, uint32_t pb)
+__host__ __device__ __forceinline__ uint32_t sel_pair(uint32_t pa, uint32_t pb)
 {
     return 0x1010u + 0x22u * pa + 0x2200u * pb;
 }
@@ -77,8 +92,8 @@ __device__ __forceinline__ uint32_t sel_pair(uint32_t pa, uint32_t pb)
 // fp16 lanes pa and pb (0..7) of the four words {d, c, b, a} -> one half2.
 // Two permutes take the lanes' positions within each half of the group, a
 // third picks the half each lane lives in.
-__device__ __forceinline__ uint32_t gather_pair8(uint32_t a, uint32_t b, uint32_t c,
-                                                 uint32_t d, uint32_t pa, uint32_t pb)
+__host__ __device__ __forceinline__ uint32_t gather_pair8(uint32_t a, uint32_t b, uint32_t c,
+                                                          uint32_t d, uint32_t pa, uint32_t pb)
 {
     const uint32_t s = sel_pair(pa & 3u, pb & 3u);
     const uint32_t lo = prmt(a, b, s);
@@ -89,10 +104,11 @@ __device__ __forceinline__ uint32_t gather_pair8(uint32_t a, uint32_t b, uint32_
 
 // ---------------------------------------------------------------- math
 // acc + v.lo*x.lo + v.hi*x.hi with fp16 operands and fp32 accumulation.
-// The product of two fp16 values is exact in fp32, so each step rounds once.
-__device__ __forceinline__ float fma_h2(uint32_t v, uint32_t x, float acc)
+// The product of two fp16 values is exact in fp32, so each step rounds once
+// (on the host too, where fmaf of the converted operands does the same).
+__host__ __device__ __forceinline__ float fma_h2(uint32_t v, uint32_t x, float acc)
 {
-#if NM_USE_MIXED_FMA
+#if defined(__CUDA_ARCH__) && NM_USE_MIXED_FMA
     asm("{\n\t.reg .f16 vl, vh, xl, xh;\n\t"
         "mov.b32 {vl, vh}, %1;\n\t"
         "mov.b32 {xl, xh}, %2;\n\t"

@@ -65,7 +65,7 @@ template <> struct Pattern<2, 4> {
     static constexpr int CK = 16;
     using mask_t = uint16_t;
     struct Sel { uint32_t s[4]; };
-    __device__ static __forceinline__ Sel decode(uint32_t m)
+    __host__ __device__ static __forceinline__ Sel decode(uint32_t m)
     {
         const uint32_t idx = m & 0x7777u;
         const uint32_t first = prmt(0x10321010u, 0x10321054u, idx);   // lane of the lower kept k
@@ -74,7 +74,7 @@ template <> struct Pattern<2, 4> {
         const uint32_t s23 = prmt(first, second, 0x7362u);
         return Sel{{s01, s01 >> 16, s23, s23 >> 16}};
     }
-    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
+    __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         acc = fma_h2(v.x, prmt(x[0], x[1], sel.s[0]), acc);
@@ -90,13 +90,13 @@ template <> struct Pattern<1, 4> {
     static constexpr int CK = 32;
     using mask_t = uint32_t;
     struct Sel { uint32_t s[4]; };
-    __device__ static __forceinline__ Sel decode(uint32_t m)
+    __host__ __device__ static __forceinline__ Sel decode(uint32_t m)
     {
         const uint32_t lo = prmt(0x10321076u, 0x10101054u, m & 0x7777u);
         const uint32_t hi = prmt(0x10321076u, 0x10101054u, (m >> 16) & 0x7777u);
         return Sel{{lo, lo >> 16, hi, hi >> 16}};
     }
-    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
+    __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
@@ -115,7 +115,7 @@ template <> struct Pattern<1, 4> {
 // gather8(): a permute of words 0-1 and one of words 2-3 by the lanes'
 // positions within a half, then a permute picking the half each lives in.
 struct Pair8 { uint32_t s, pick; };
-__device__ __forceinline__ Pair8 pair8(uint32_t pa, uint32_t pb)
+__host__ __device__ __forceinline__ Pair8 pair8(uint32_t pa, uint32_t pb)
 {
     // Both selectors at once from q = pa | pb << 8: the within-half lane of
     // each (bits 0-1 of each byte) scales the sel_pair step 0x22, the half
@@ -123,20 +123,20 @@ __device__ __forceinline__ Pair8 pair8(uint32_t pa, uint32_t pb)
     const uint32_t q = pa | (pb << 8);
     return Pair8{0x1010u + 0x22u * (q & 0x0303u), 0x3210u + 0x44u * ((q >> 2) & 0x0101u)};
 }
-__device__ __forceinline__ uint32_t gather8(const uint32_t *xg, const Pair8 &p)
+__host__ __device__ __forceinline__ uint32_t gather8(const uint32_t *xg, const Pair8 &p)
 {
     return prmt(prmt(xg[0], xg[1], p.s), prmt(xg[2], xg[3], p.s), p.pick);
 }
 // Position of the lowest / highest set bit of a nonzero byte (one
 // find-leading-one each; the lowest set bit is isolated with b & -b).
-__device__ __forceinline__ uint32_t lowest(uint32_t b) { return msb(b & (0u - b)); }
+__host__ __device__ __forceinline__ uint32_t lowest(uint32_t b) { return msb(b & (0u - b)); }
 
 // 2:8 -- four groups of 8 per chunk, one value pair per group.
 template <> struct Pattern<2, 8> {
     static constexpr int CK = 32;
     using mask_t = uint32_t;
     struct Sel { Pair8 p[4]; };
-    __device__ static __forceinline__ Sel decode(uint32_t m)
+    __host__ __device__ static __forceinline__ Sel decode(uint32_t m)
     {
         Sel s;
 #pragma unroll
@@ -146,7 +146,7 @@ template <> struct Pattern<2, 8> {
         }
         return s;
     }
-    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
+    __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
@@ -162,7 +162,7 @@ template <> struct Pattern<4, 8> {
     static constexpr int CK = 16;
     using mask_t = uint16_t;
     struct Sel { Pair8 p[4]; };
-    __device__ static __forceinline__ Sel decode(uint32_t m)
+    __host__ __device__ static __forceinline__ Sel decode(uint32_t m)
     {
         Sel s;
 #pragma unroll
@@ -177,7 +177,7 @@ template <> struct Pattern<4, 8> {
         }
         return s;
     }
-    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
+    __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         acc = fma_h2(v.x, gather8(x, sel.p[0]), acc);
@@ -193,7 +193,7 @@ template <> struct Pattern<1, 8> {
     static constexpr int CK = 64;
     using mask_t = uint64_t;
     struct Sel { uint32_t pa[4], pb[4]; };
-    __device__ static __forceinline__ Sel decode(uint64_t m)
+    __host__ __device__ static __forceinline__ Sel decode(uint64_t m)
     {
         Sel s;
 #pragma unroll
@@ -204,7 +204,7 @@ template <> struct Pattern<1, 8> {
         }
         return s;
     }
-    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
+    __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
@@ -227,8 +227,8 @@ template <int M> struct DensePattern {  // N == M: every position kept, mask not
     static constexpr int CK = 8;
     using mask_t = uint8_t;
     struct Sel {};
-    __device__ static __forceinline__ Sel decode(uint32_t) { return Sel{}; }
-    __device__ static __forceinline__ float dot(const uint4 &v, const Sel &, const uint32_t *x,
+    __host__ __device__ static __forceinline__ Sel decode(uint32_t) { return Sel{}; }
+    __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &, const uint32_t *x,
                                                 float acc)
     {
         acc = fma_h2(v.x, x[0], acc);

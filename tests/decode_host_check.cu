@@ -1,0 +1,118 @@
+// Host-side check of the vectorised kernels' mask decode and lane gather
+// (Pattern<N, M>::decode and ::dot from csrc/nm_fast.cuh, compiled for the
+// CPU).  Built and run by tests/test_decode_host.py; no GPU is used.
+//
+// For every valid mask of one 16-byte value chunk (all of them for 2:4, 1:4,
+// 2:8 and 4:8, a seeded sample for 1:8) and every value slot i of the chunk,
+// dot() is called with a one-hot value vector (slot i = 1.0, the others 0)
+// and x lane p = p + 1: the result must be 1 + the position of the chunk's
+// i-th kept weight, the positions taken group by group in increasing k (the
+// packed layout's fixed-step order).  The dense patterns (N = M) keep every
+// position.
+#include <cstdint>
+#include <cstdio>
+#include <vector>
+
+#include "nm_fast.cuh"
+
+namespace {
+
+uint16_t f16_of_int(int v)  // exact for 0 <= v <= 2048
+{
+    if (v == 0) return 0;
+    int e = 0;
+    while ((v >> e) > 1) ++e;
+    const uint32_t frac = (static_cast<uint32_t>(v) << (10 - e)) & 0x3FFu;
+    return static_cast<uint16_t>(((e + 15) << 10) | frac);
+}
+
+struct Result { long checks = 0, fails = 0; };
+
+template <int N, int M>
+void check_mask(uint64_t mask, Result &r)
+{
+    using P = nm::Pattern<N, M>;
+    constexpr int CK = P::CK;
+    // kept positions in order: groups in order, increasing k inside a group
+    std::vector<int> kept;
+    for (int p = 0; p < CK; ++p)
+        if (N == M || ((mask >> p) & 1u)) kept.push_back(p);
+    if (static_cast<int>(kept.size()) != 8) {
+        std::printf("internal: %zu kept positions\n", kept.size());
+        ++r.fails;
+        return;
+    }
+    uint32_t x[CK / 2];
+    for (int w = 0; w < CK / 2; ++w)
+        x[w] = f16_of_int(2 * w + 1) | (static_cast<uint32_t>(f16_of_int(2 * w + 2)) << 16);
+    const auto sel = P::decode(static_cast<typename P::mask_t>(mask));
+    for (int i = 0; i < 8; ++i) {
+        uint32_t vw[4] = {0, 0, 0, 0};
+        vw[i / 2] = static_cast<uint32_t>(0x3C00u) << (16 * (i % 2));
+        const uint4 v = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+        const float got = P::dot(v, sel, x, 0.0f);
+        ++r.checks;
+        if (got != static_cast<float>(kept[i] + 1)) {
+            if (r.fails < 5)
+                std::printf("%d:%d mask %016llx slot %d: got %g, want %d\n", N, M,
+                            static_cast<unsigned long long>(mask), i, got, kept[i] + 1);
+            ++r.fails;
+        }
+    }
+}
+
+// Every group mask of width M with exactly N set bits.
+std::vector<uint32_t> group_masks(int N, int M)
+{
+    std::vector<uint32_t> out;
+    for (uint32_t g = 0; g < (1u << M); ++g)
+        if (__builtin_popcount(g) == N) out.push_back(g);
+    return out;
+}
+
+template <int N, int M>
+Result check_all(long sample)
+{
+    Result r;
+    constexpr int groups = nm::Pattern<N, M>::CK / M;
+    const std::vector<uint32_t> gm = group_masks(N, M);
+    long total = 1;
+    for (int g = 0; g < groups; ++g) total *= static_cast<long>(gm.size());
+    uint64_t state = 0x9E3779B97F4A7C15ull;
+    const bool all = sample <= 0 || total <= sample;
+    const long count = all ? total : sample;
+    for (long t = 0; t < count; ++t) {
+        long idx = t;
+        if (!all) {  // xorshift64 sample of the combinations
+            state ^= state << 13;
+            state ^= state >> 7;
+            state ^= state << 17;
+            idx = static_cast<long>(state % static_cast<uint64_t>(total));
+        }
+        uint64_t mask = 0;
+        for (int g = 0; g < groups; ++g) {
+            mask |= static_cast<uint64_t>(gm[idx % gm.size()]) << (M * g);
+            idx /= static_cast<long>(gm.size());
+        }
+        check_mask<N, M>(mask, r);
+    }
+    std::printf("%d:%d %ld masks%s, %ld checks, %ld failures\n", N, M, count,
+                all ? " (all)" : " (sampled)", r.checks, r.fails);
+    return r;
+}
+
+}  // namespace
+
+int main()
+{
+    long fails = 0;
+    fails += check_all<2, 4>(0).fails;
+    fails += check_all<1, 4>(0).fails;
+    fails += check_all<2, 8>(0).fails;
+    fails += check_all<4, 8>(0).fails;
+    fails += check_all<1, 8>(300000).fails;
+    fails += check_all<4, 4>(0).fails;
+    fails += check_all<8, 8>(0).fails;
+    std::printf(fails ? "FAIL\n" : "OK\n");
+    return fails ? 1 : 0;
+}
