@@ -9,11 +9,17 @@
 // i-th kept weight, the positions taken group by group in increasing k (the
 // packed layout's fixed-step order).  The dense patterns (N = M) keep every
 // position.
+//
+// It also checks the tensor-core product's group expansion (expand_sel in
+// csrc/nm_tc_expand.cuh, used as the two 16-bit selectors the kernel
+// stores): for every 2:4 nibble, the group's value pair lands on its two
+// kept positions, lower k first, and the other two positions are zero.
 #include <cstdint>
 #include <cstdio>
 #include <vector>
 
 #include "nm_fast.cuh"
+#include "nm_tc_expand.cuh"
 
 namespace {
 
@@ -101,6 +107,29 @@ Result check_all(long sample)
     return r;
 }
 
+Result check_expand()
+{
+    Result r;
+    const uint32_t lo = 0x1357u, hi = 0x2468u, v = lo | (hi << 16);
+    for (uint32_t n : group_masks(2, 4)) {
+        const uint32_t sel = nm::expand_sel(n);
+        const uint32_t w[2] = {nm::prmt(v, 0u, sel & 0xFFFFu), nm::prmt(v, 0u, sel >> 16)};
+        int j = 0;
+        for (int p = 0; p < 4; ++p) {
+            const uint32_t want = ((n >> p) & 1u) ? (j++ == 0 ? lo : hi) : 0u;
+            const uint32_t got = (w[p / 2] >> (16 * (p % 2))) & 0xFFFFu;
+            ++r.checks;
+            if (got != want) {
+                std::printf("expand nibble %x position %d: got %04x, want %04x\n", n, p, got, want);
+                ++r.fails;
+            }
+        }
+    }
+    std::printf("2:4x expand %zu nibbles, %ld checks, %ld failures\n", group_masks(2, 4).size(),
+                r.checks, r.fails);
+    return r;
+}
+
 }  // namespace
 
 int main()
@@ -113,6 +142,7 @@ int main()
     fails += check_all<1, 8>(300000).fails;
     fails += check_all<4, 4>(0).fails;
     fails += check_all<8, 8>(0).fails;
+    fails += check_expand().fails;
     std::printf(fails ? "FAIL\n" : "OK\n");
     return fails ? 1 : 0;
 }

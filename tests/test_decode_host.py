@@ -2,7 +2,8 @@
 tests/decode_host_check.cu for the host with nvcc (the product's
 Pattern<N, M>::decode and ::dot compiled for the CPU) and runs it over every
 valid chunk mask of 2:4, 1:4, 2:8, 4:8 and the dense patterns, and a sample
-of 1:8.  No GPU is used."""
+of 1:8; and the tensor-core product's 2:4 group expansion table.  No GPU is
+used."""
 import os
 import shutil
 import subprocess
@@ -34,6 +35,6 @@ def test_mask_decode_and_gather_on_the_host(tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert run.returncode == 0 and run.stdout.strip().endswith("OK"), run.stdout + run.stderr
     # every pattern reported, none with failures
-    for pat in ("2:4", "1:4", "2:8", "4:8", "1:8", "4:4", "8:8"):
+    for pat in ("2:4", "1:4", "2:8", "4:8", "1:8", "4:4", "8:8", "2:4x"):
         line = [l for l in run.stdout.splitlines() if l.startswith(pat + " ")]
         assert line and line[0].endswith(" 0 failures"), run.stdout
