@@ -1,0 +1,161 @@
+// Host-side check of the streaming kernels' launch planning (rows_plan,
+// rows_plan_group and bulk_plan from csrc/nm_bulk_plan.cu, compiled for and
+// run on the CPU).  Built and run by tests/test_plan_host.py; no GPU is used.
+//
+// Over the decode-layer shapes of the workloads, ragged shapes, every vector
+// count 1-8 and every chunk span (CK = 8, 16, 32, 64), each plan must:
+//   * fit the shared-memory limit, with every region 16-byte aligned;
+//   * cover K exactly: K tiles and their segments tile the row's chunks with
+//     no gap and no chunk twice (tiles and segments of a multiple of 32
+//     chunks when cut);
+//   * cover the rows: grid CTAs of ceil(rows / grid) rows, at most one CTA
+//     per row; a group's CTAs split in order, at least one per matrix and
+//     at most one per row;
+//   * keep the per-lane partial sums (R rows x B vectors) within the
+//     kernel's register budget, and the carried partial sums within 64 KB.
+#include <cstdint>
+#include <cstdio>
+#include <vector>
+
+#include "nm_bulk.cuh"
+#include "nm_rows.cuh"
+
+namespace {
+
+constexpr int kNsm = 148;
+constexpr int kMaxSmem = 232448;  // opt-in shared memory per CTA on sm_103a
+long g_fail = 0, g_plans = 0, g_none = 0;
+
+#define EXPECT(cond, ...)                                                   \
+    do {                                                                    \
+        if (!(cond)) {                                                      \
+            if (g_fail < 20) {                                              \
+                std::printf("FAIL %s: ", #cond);                            \
+                std::printf(__VA_ARGS__);                                   \
+                std::printf("\n");                                          \
+            }                                                               \
+            ++g_fail;                                                       \
+        }                                                                   \
+    } while (0)
+
+void check_rows_plan(const nm::RowsPlan &p, int64_t rows_per_cta, int chunks, int CK, int B,
+                     const char *what)
+{
+    const int MB = CK / 8;
+    EXPECT(p.smem <= static_cast<size_t>(kMaxSmem), "%s smem %zu", what, p.smem);
+    EXPECT(p.W >= 1 && p.W <= nm::kRowsMaxWarps, "%s W %d", what, p.W);
+    EXPECT(p.SW >= 2 && p.SW <= 4, "%s SW %d", what, p.SW);
+    // K tiles
+    EXPECT(p.ktiles >= 1 && static_cast<int64_t>(p.ktiles) * p.tile_chunks >= chunks &&
+               static_cast<int64_t>(p.ktiles - 1) * p.tile_chunks < chunks,
+           "%s ktiles %d tile %d chunks %d", what, p.ktiles, p.tile_chunks, chunks);
+    EXPECT(p.ktiles == 1 || p.tile_chunks % 32 == 0, "%s tile %d", what, p.tile_chunks);
+    const int last = chunks - (p.ktiles - 1) * p.tile_chunks;
+    // segments of a tile and of the last tile
+    EXPECT(p.nseg >= 1 && static_cast<int64_t>(p.nseg) * p.seg_chunks >= p.tile_chunks &&
+               static_cast<int64_t>(p.nseg - 1) * p.seg_chunks < p.tile_chunks,
+           "%s nseg %d seg %d tile %d", what, p.nseg, p.seg_chunks, p.tile_chunks);
+    EXPECT(p.nseg_last >= 1 && static_cast<int64_t>(p.nseg_last) * p.seg_chunks >= last &&
+               static_cast<int64_t>(p.nseg_last - 1) * p.seg_chunks < last,
+           "%s nseg_last %d seg %d last %d", what, p.nseg_last, p.seg_chunks, last);
+    EXPECT(p.nseg == 1 || p.seg_chunks % 32 == 0, "%s seg %d", what, p.seg_chunks);
+    // slot layout: one row's segment of values and of mask bytes
+    EXPECT(p.seg_v == p.seg_chunks * 16, "%s seg_v", what);
+    EXPECT(p.seg_m >= p.seg_chunks * MB && p.seg_m % 16 == 0 && p.seg_m < p.seg_chunks * MB + 16,
+           "%s seg_m %d", what, p.seg_m);
+    EXPECT(p.stage_bytes == p.R * (p.seg_v + p.seg_m), "%s stage", what);
+    EXPECT(p.R >= 1 && p.R <= nm::rows_rmax(B) && p.R * B <= 16, "%s R %d B %d", what, p.R, B);
+    // x buffer: B vectors of the tile's positions, fp16
+    EXPECT(p.xbuf_bytes == B * p.tile_chunks * CK * 2, "%s xbuf", what);
+    // regions in order, 16-byte aligned, inside smem
+    const int S = p.SW * p.W;
+    EXPECT(p.off_x == S * p.stage_bytes, "%s off_x", what);
+    EXPECT(p.off_bar == p.off_x + (p.ktiles > 1 ? 2 : 1) * p.xbuf_bytes, "%s off_bar", what);
+    EXPECT(p.off_carry >= p.off_bar + 8 * S, "%s off_carry", what);
+    EXPECT(p.off_x % 16 == 0 && p.off_bar % 16 == 0 && p.off_carry % 16 == 0 &&
+               p.stage_bytes % 16 == 0 && p.xbuf_bytes % 16 == 0,
+           "%s alignment", what);
+    const int64_t carry = p.ktiles > 1 ? rows_per_cta * B * 4 : 0;
+    EXPECT(carry <= 64 * 1024, "%s carry %lld", what, static_cast<long long>(carry));
+    EXPECT(static_cast<int64_t>(p.off_carry) + carry <= static_cast<int64_t>(p.smem),
+           "%s carry region", what);
+}
+
+void one(int64_t rows, int64_t K, int N, int M, int B)
+{
+    const int CK = 8 * M / N;
+    if (K % CK != 0) return;
+    const int chunks = static_cast<int>(K / CK);
+    char what[128];
+    std::snprintf(what, sizeof(what), "rows %lld K %lld %d:%d B %d", static_cast<long long>(rows),
+                  static_cast<long long>(K), N, M, B);
+    nm::RowsPlan p;
+    if (nm::rows_plan(rows, chunks, CK, B, kNsm, kMaxSmem, nm::kRowsMaxWarps, &p)) {
+        ++g_plans;
+        EXPECT(p.grid >= 1 && p.grid <= rows, "%s grid %d", what, p.grid);
+        const int64_t rpc = (rows + p.grid - 1) / p.grid;
+        EXPECT(rpc * p.grid >= rows && (rpc - 1) * p.grid < rows, "%s rpc", what);
+        check_rows_plan(p, rpc, chunks, CK, B, what);
+    } else {
+        ++g_none;
+        // the chunk-column kernel must then take it
+        nm::BulkPlan b;
+        const bool ok = nm::bulk_plan(rows, chunks, CK, B, kNsm, kMaxSmem, &b);
+        EXPECT(ok, "%s: no plan at all", what);
+        if (ok) EXPECT(b.smem <= static_cast<size_t>(kMaxSmem), "%s bulk smem", what);
+    }
+}
+
+void group(const std::vector<int64_t> &rows, int64_t K, int N, int M, int B)
+{
+    const int CK = 8 * M / N;
+    const int chunks = static_cast<int>(K / CK);
+    char what[128];
+    std::snprintf(what, sizeof(what), "group of %zu, K %lld %d:%d B %d", rows.size(),
+                  static_cast<long long>(K), N, M, B);
+    nm::RowsPlan p;
+    int cta_begin[nm::kRowsMaxGroup + 1];
+    if (!nm::rows_plan_group(rows.data(), static_cast<int>(rows.size()), chunks, CK, B, kNsm,
+                             kMaxSmem, nm::kRowsMaxWarps, &p, cta_begin)) {
+        ++g_none;
+        return;
+    }
+    ++g_plans;
+    int64_t total = 0;
+    for (int64_t r : rows) total += r;
+    EXPECT(cta_begin[0] == 0 && cta_begin[rows.size()] == p.grid, "%s grid %d", what, p.grid);
+    const int64_t ctas = static_cast<int64_t>(kNsm) * nm::bulk_tuning().ctas_per_sm;
+    EXPECT(p.grid == static_cast<int>(std::min<int64_t>(total, ctas)), "%s grid %d", what, p.grid);
+    int64_t rpc = 0;
+    for (size_t i = 0; i < rows.size(); ++i) {
+        const int g = cta_begin[i + 1] - cta_begin[i];
+        EXPECT(g >= 1 && g <= rows[i], "%s matrix %zu gets %d CTAs", what, i, g);
+        if (g >= 1) rpc = std::max<int64_t>(rpc, (rows[i] + g - 1) / g);
+    }
+    check_rows_plan(p, rpc, chunks, CK, B, what);
+}
+
+}  // namespace
+
+int main()
+{
+    const int pats[][2] = {{2, 4}, {4, 8}, {1, 4}, {2, 8}, {1, 8}, {4, 4}, {8, 8}};
+    const int64_t rows_list[] = {1, 7, 77, 148, 149, 300, 1024, 4096, 5120, 8192, 14336,
+                                 17408, 25600, 28672, 37000, 100000};
+    const int64_t k_list[] = {128, 1024, 3072, 4096, 5120, 8192, 14336, 17408, 25600, 28672,
+                              36864, 40960, 81920};
+    for (auto &pm : pats)
+        for (int64_t r : rows_list)
+            for (int64_t K : k_list)
+                for (int B = 1; B <= 8; ++B) one(r, K, pm[0], pm[1], B);
+    const std::vector<std::vector<int64_t>> groups = {
+        {4096, 1024, 1024}, {14336, 14336}, {28672, 28672}, {8192, 1024, 1024},
+        {25600, 25600}, {333, 77, 250, 4, 5, 6, 7, 900}, {1, 1}, {100000, 1}, {700, 300, 1}};
+    for (auto &g : groups)
+        for (int64_t K : {1024L, 4096L, 5120L, 8192L})
+            for (int B = 1; B <= 8; ++B) group(g, K, 2, 4, B);
+    std::printf("%ld plans checked, %ld shapes without a row plan, %ld failures\n", g_plans,
+                g_none, g_fail);
+    std::printf(g_fail ? "FAIL\n" : "OK\n");
+    return g_fail ? 1 : 0;
+}
