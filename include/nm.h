@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 140 /* 1.4.0 */
+#define NM_VERSION 150 /* 1.5.0 */
 #define NM_MAX_BATCH 8
 #define NM_MAX_GROUP 8
 
