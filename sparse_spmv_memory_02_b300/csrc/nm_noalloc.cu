@@ -12,9 +12,12 @@
 //
 // The scratch array lives in this file; its device address is looked up
 // once per device (cudaGetSymbolAddress on the first call made with that
-// device current) and cached.  The array is shared by every call on a
+// device current) and cached, so the library must not be called on a device
+// again after cudaDeviceReset.  The array is shared by every call on a
 // device and keeps the last call's contents, so each call clears it first;
 // two calls that overlap on the GPU (for example on two streams) race on it.
+// Like nm_pack, the call synchronises its stream, so a capturing stream is
+// refused.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -83,10 +86,20 @@ extern "C" nm_status nm_pack_noalloc(const void *W, const uint8_t *mask, int64_t
         reinterpret_cast<uintptr_t>(masks) % 16 != 0)
         return noalloc_fail(NM_ERR_INVALID_ARG, "values and masks must be 16-byte aligned");
 
-    unsigned int *d_bad = nullptr;
-    cudaError_t e = scratch_for_current_device(&d_bad);
-    if (e != cudaSuccess) return noalloc_fail(NM_ERR_CUDA, cudaGetErrorString(e));
+    // The call synchronises its stream to read the counter back, which a
+    // capturing stream forbids: refuse it before any work is queued, so the
+    // caller's capture stays valid.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return noalloc_fail(NM_ERR_CUDA, cudaGetErrorString(e));
+    if (cap != cudaStreamCaptureStatusNone)
+        return noalloc_fail(NM_ERR_INVALID_ARG,
+                            "nm_pack_noalloc synchronises its stream and cannot be captured");
+
+    unsigned int *d_bad = nullptr;
+    e = scratch_for_current_device(&d_bad);
+    if (e != cudaSuccess) return noalloc_fail(NM_ERR_CUDA, cudaGetErrorString(e));
     unsigned int h_bad = 0;
     e = cudaMemsetAsync(d_bad, 0, sizeof(unsigned int), s);
     if (e == cudaSuccess)
