@@ -39,6 +39,11 @@
  *     no effect.  A failing CUDA call returns NM_ERR_CUDA.  nm_last_error()
  *     then describes the failure.  No C++ exception crosses this interface.
  *   - rows == 0 is an empty problem: the call succeeds and does nothing.
+ *   - Per-device state: on its first use on a device the library caches
+ *     device attributes and the device addresses of its static device
+ *     variables (the error word, nm_pack_noalloc's scratch).  After
+ *     cudaDeviceReset on a device, libnm must not be called on that device
+ *     again in the same process.
  */
 #ifndef NM_H_
 #define NM_H_
@@ -125,9 +130,12 @@ nm_status nm_pack(const void *W, const uint8_t *mask, int64_t rows, int64_t K,
  *   Arguments, layout, results and errors are those of nm_pack, plus:
  *   - rows*(K/M) above NM_PACK_NOALLOC_MAX_GROUPS (what the 32-bit counter
  *     can count) is rejected with NM_ERR_INVALID_ARG;
+ *   - like nm_pack it SYNCHRONISES `stream` to read the counter back, so it
+ *     cannot be captured in a CUDA graph: a capturing stream is refused with
+ *     NM_ERR_INVALID_ARG before anything is queued (the capture stays valid);
  *   - the first call on a device, made with that device current, looks up
- *     the array's device address (cudaGetSymbolAddress) and caches it; make
- *     that first call before any stream capture;
+ *     the array's device address (cudaGetSymbolAddress) and caches it (see
+ *     "Per-device state" above);
  *   - every call on a device shares the array and clears the counter first;
  *     two calls that overlap on the GPU (for example on different streams)
  *     race on it and may report wrong counts.
@@ -161,9 +169,12 @@ nm_status nm_unpack(const nm_matrix *A, void *W_out, nm_stream_t stream);
  * dependent launch, so it may start streaming A's packed arrays while the
  * kernel before it in `stream` is still running; it reads x and writes y only
  * after that kernel has completed.  A's arrays must therefore not be written
- * by the kernel immediately before the call (nm_pack, which synchronises,
- * and copies are fine).  NM_BULK_TUNE=pdl=0 in the environment turns this
- * off.
+ * by the kernel immediately before the call.  The library's own writers are
+ * safe to precede it: nm_pack and nm_pack_noalloc synchronise, and
+ * nm_prune_pack ends with a launch that does not overlap.  A caller's own
+ * kernel that writes the packed arrays needs something in between (an event
+ * wait, a memcpy, or any ordinary kernel launch).  NM_BULK_TUNE=pdl=0 in the
+ * environment turns the overlap off.
  */
 nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
                   nm_stream_t stream);
@@ -259,7 +270,11 @@ nm_status nm_select_mask(const void *W, const float *col_scale, int64_t rows, in
  * (values, masks as for nm_pack) of W pruned by the same rule, without the
  * u8 mask.  Same arguments and errors as nm_select_mask, values and masks as
  * nm_pack (16-byte aligned).  Asynchronous, allocates nothing, capturable
- * (unlike nm_pack it has no invalid groups to report).
+ * (unlike nm_pack it has no invalid groups to report).  An nm_spmv* call
+ * made right after it on the same stream may read the packed arrays it
+ * writes: the call ends with an ordinary (non-overlapping) launch, so the
+ * next call's early weight copies (see nm_spmv) start only after the packed
+ * arrays are complete.
  */
 nm_status nm_prune_pack(const void *W, const float *col_scale, int64_t rows, int64_t K, int N,
                         int M, void *values, uint32_t *masks, nm_stream_t stream);

@@ -257,6 +257,10 @@ cudaError_t launch_select(const uint16_t *W, const float *scale, int64_t rows, i
     return cudaGetLastError();
 }
 
+// Empty kernel: a stream-ordered boundary that a programmatic dependent
+// launch after it cannot cross (see launch_prune_pack).
+__global__ void nm_stream_fence_kernel() {}
+
 cudaError_t launch_prune_pack(const uint16_t *W, const float *scale, int64_t rows, int64_t K,
                               int N, int M, uint16_t *values, uint32_t *masks, cudaStream_t s)
 {
@@ -266,6 +270,14 @@ cudaError_t launch_prune_pack(const uint16_t *W, const float *scale, int64_t row
         nm_prune_pack_kernel<4><<<grid, 256, 0, s>>>(W, scale, rows, K, N, values, masks);
     else
         nm_prune_pack_kernel<8><<<grid, 256, 0, s>>>(W, scale, rows, K, N, values, masks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // The packed arrays just written are what an SpMV launched next on this
+    // stream reads, and the SpMV kernels start copying weights before their
+    // dependence wait (programmatic dependent launch).  An ordinary launch
+    // between the two starts only once the pack has completed and its writes
+    // are visible, and the SpMV can overlap only that launch.
+    nm_stream_fence_kernel<<<1, 32, 0, s>>>();
     return cudaGetLastError();
 }
 

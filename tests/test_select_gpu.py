@@ -92,3 +92,42 @@ def test_select_graph_capture_and_empty():
     e = torch.empty(0, 64, dtype=torch.float16, device=DEV)
     assert nm.nm_select_mask(e, 2, 4).shape == (0, 64)
     assert nm.nm_prune_pack(e, 2, 4).rows == 0
+
+
+@pytest.mark.parametrize("graph", [False, True])
+@pytest.mark.parametrize("batch", [1, 4])
+def test_prune_pack_then_spmv_without_sync(graph, batch):
+    """nm_prune_pack followed at once by an SpMV on the same stream (no host
+    synchronisation, eager or in one CUDA graph): the SpMV, whose weight
+    copies may start before its dependence wait, must read the arrays the
+    prune-pack just wrote, not what the buffers held before."""
+    rows, K, N, M = 4096, 4096, 2, 4
+    W, scale = _inputs(rows, K, 11, True)
+    W_old, _ = _inputs(rows, K, 12, False)
+    A = nm.nm_prune_pack(W_old, N, M)  # the buffers first hold another matrix
+    x = nm_synth.activations(K, batch, 13, True, DEV)
+    y = torch.empty(batch, rows, dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+
+    def run():
+        nm.nm_prune_pack(W, N, M, scale, values=A.values, masks=A.masks)
+        nm.nm_spmv_batched(A, x, y)
+
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                run()
+        torch.cuda.current_stream().wait_stream(side)
+        nm.nm_prune_pack(W_old, N, M, values=A.values, masks=A.masks)  # stale again
+        g.replay()
+    else:
+        run()
+    torch.cuda.synchronize()
+    Wn = _np16(W)
+    mref = oracle.select_mask(Wn, N, M, scale.cpu().numpy())
+    yr, sr = oracle.spmv_dense(Wn, mref, _np16(x))
+    assert oracle.within_tolerance(y.double().cpu().numpy(), yr, sr).all()
+    assert nm.nm_device_errors() == 0
