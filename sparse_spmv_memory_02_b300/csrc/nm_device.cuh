@@ -59,12 +59,18 @@ __device__ __forceinline__ uint4 ld_keep_v4(const uint4 *p)
 
 // ---------------------------------------------------------------- bits
 // Byte permute: result byte i = byte (sel >> 4i) & 7 of the 8-byte {hi, lo}.
+// Every selector in this library keeps bit 3 of each nibble clear, so the
+// PTX instruction is used as is: __byte_perm ignores that bit by definition,
+// which costs a masking instruction per permute whose selector is not a
+// compile-time constant.  Bits 16-31 of sel are ignored.
 // The bit helpers below also compile for the host (the same results, so the
 // mask decode can be checked on a machine without a GPU).
 __host__ __device__ __forceinline__ uint32_t prmt(uint32_t lo, uint32_t hi, uint32_t sel)
 {
 #ifdef __CUDA_ARCH__
-    return __byte_perm(lo, hi, sel);
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(sel));
+    return r;
 #else
     const uint64_t b = (static_cast<uint64_t>(hi) << 32) | lo;
     uint32_t r = 0;

@@ -54,14 +54,27 @@ namespace nm {
 //                packed two per word (XR = CK/2 words).
 // Results for groups without exactly N set bits are unspecified; the mask
 // only ever feeds byte permutes and selects, never an address.
+//
+//   decode_tab(m, tab): the same Sel, for kernels that hold a per-CTA decode
+//                table in shared memory: kTabWords 32-bit words, word i =
+//                tab_entry(i).  The 8-wide patterns look each group's byte
+//                up in a 256-word table (one shared load replaces a chain of
+//                bit scans and selector arithmetic); the others ignore tab.
+//                An invalid group byte reads a defined word of the table.
 
 template <int N, int M> struct Pattern;
+
+// For patterns decoded from registers alone.
+struct NoTable {
+    static constexpr int kTabWords = 0;
+    __host__ __device__ static constexpr uint32_t tab_entry(uint32_t) { return 0; }
+};
 
 // 2:4 -- four groups per chunk, one value pair per group.  A valid nibble
 // has exactly two set bits, so its low three bits already identify it; two
 // 8-entry byte tables (held in immediates, indexed by byte permutes) map
 // those bits to the selector bytes of the first and second kept lane.
-template <> struct Pattern<2, 4> {
+template <> struct Pattern<2, 4> : NoTable {
     static constexpr int CK = 16;
     using mask_t = uint16_t;
     struct Sel { uint32_t s[4]; };
@@ -73,6 +86,10 @@ template <> struct Pattern<2, 4> {
         const uint32_t s01 = prmt(first, second, 0x5140u);
         const uint32_t s23 = prmt(first, second, 0x7362u);
         return Sel{{s01, s01 >> 16, s23, s23 >> 16}};
+    }
+    __host__ __device__ static __forceinline__ Sel decode_tab(uint32_t m, const uint32_t *)
+    {
+        return decode(m);
     }
     __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
@@ -86,7 +103,7 @@ template <> struct Pattern<2, 4> {
 
 // 1:4 -- eight groups per chunk; a value pair spans two groups.  A valid
 // nibble has one set bit and its low three bits identify it (8 -> 0).
-template <> struct Pattern<1, 4> {
+template <> struct Pattern<1, 4> : NoTable {
     static constexpr int CK = 32;
     using mask_t = uint32_t;
     struct Sel { uint32_t s[4]; };
@@ -95,6 +112,10 @@ template <> struct Pattern<1, 4> {
         const uint32_t lo = prmt(0x10321076u, 0x10101054u, m & 0x7777u);
         const uint32_t hi = prmt(0x10321076u, 0x10101054u, (m >> 16) & 0x7777u);
         return Sel{{lo, lo >> 16, hi, hi >> 16}};
+    }
+    __host__ __device__ static __forceinline__ Sel decode_tab(uint32_t m, const uint32_t *)
+    {
+        return decode(m);
     }
     __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
@@ -131,11 +152,17 @@ __host__ __device__ __forceinline__ uint32_t gather8(const uint32_t *xg, const P
 // find-leading-one each; the lowest set bit is isolated with b & -b).
 __host__ __device__ __forceinline__ uint32_t lowest(uint32_t b) { return msb(b & (0u - b)); }
 
-// 2:8 -- four groups of 8 per chunk, one value pair per group.
+// 2:8 -- four groups of 8 per chunk, one value pair per group.  Table word
+// g(b) = b ^ (b >> 1): the gather selectors of the lowest and the highest
+// set bit of b, s in bits 0-15 and pick in bits 16-31.  Indexed by b itself
+// the 28 valid bytes would crowd into six of the 32 shared-memory banks (3
+// to a bank); their Gray codes g(b) fall at most 2 to a bank, and one shift
+// and one logic op give g of all four group bytes of a chunk at once.
 template <> struct Pattern<2, 8> {
     static constexpr int CK = 32;
     using mask_t = uint32_t;
     struct Sel { Pair8 p[4]; };
+    static constexpr int kTabWords = 256;
     __host__ __device__ static __forceinline__ Sel decode(uint32_t m)
     {
         Sel s;
@@ -143,6 +170,29 @@ template <> struct Pattern<2, 8> {
         for (int g = 0; g < 4; ++g) {
             const uint32_t b = (m >> (8 * g)) & 0xFFu;
             s.p[g] = pair8(lowest(b), msb(b));
+        }
+        return s;
+    }
+    // word i of the table: the entry of the byte whose Gray code is i
+    __host__ __device__ static uint32_t tab_entry(uint32_t i)
+    {
+        uint32_t b = i;  // inverse Gray code of an 8-bit value
+        b ^= b >> 1;
+        b ^= b >> 2;
+        b ^= b >> 4;
+        const Pair8 p = b ? pair8(lowest(b), msb(b)) : pair8(0, 0);
+        return p.s | (p.pick << 16);
+    }
+    __host__ __device__ static __forceinline__ Sel decode_tab(uint32_t m, const uint32_t *tab)
+    {
+        // Gray code of each byte: the bit shifted in from the next byte is
+        // masked off
+        const uint32_t gm = m ^ ((m >> 1) & 0x7F7F7F7Fu);
+        Sel s;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t e = tab[(gm >> (8 * g)) & 0xFFu];
+            s.p[g] = Pair8{e, e >> 16};
         }
         return s;
     }
@@ -157,11 +207,16 @@ template <> struct Pattern<2, 8> {
 };
 
 // 4:8 -- two groups of 8 per chunk, two value pairs per group: the two
-// lowest and the two highest kept positions.
+// lowest and the two highest kept positions.  Table word b: the positions
+// of the (up to) four lowest set bits of b, one a byte in increasing order
+// (0 for missing ones); the selectors of both pairs follow from it with two
+// masked multiplies, since selector byte j of a gather is 0x10 + 0x22 *
+// (p_j & 3) and pick byte j is its base + 0x44 * (p_j >> 2).
 template <> struct Pattern<4, 8> {
     static constexpr int CK = 16;
     using mask_t = uint16_t;
     struct Sel { Pair8 p[4]; };
+    static constexpr int kTabWords = 256;
     __host__ __device__ static __forceinline__ Sel decode(uint32_t m)
     {
         Sel s;
@@ -177,6 +232,28 @@ template <> struct Pattern<4, 8> {
         }
         return s;
     }
+    __host__ __device__ static uint32_t tab_entry(uint32_t b)
+    {
+        uint32_t q = 0;
+        for (int n = 0; n < 4 && b != 0; ++n) {
+            q |= lowest(b) << (8 * n);
+            b &= b - 1u;
+        }
+        return q;
+    }
+    __host__ __device__ static __forceinline__ Sel decode_tab(uint32_t m, const uint32_t *tab)
+    {
+        Sel s;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const uint32_t q = tab[(m >> (8 * g)) & 0xFFu];
+            const uint32_t sel = (q & 0x03030303u) * 0x22u + 0x10101010u;
+            const uint32_t pick = (q & 0x04040404u) * 0x11u + 0x32103210u;
+            s.p[2 * g] = Pair8{sel, pick};
+            s.p[2 * g + 1] = Pair8{sel >> 16, pick >> 16};
+        }
+        return s;
+    }
     __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
     {
@@ -189,7 +266,7 @@ template <> struct Pattern<4, 8> {
 
 // 1:8 -- eight groups of 8 per chunk; a value pair spans two groups.  The
 // single set bit of a group is its highest.
-template <> struct Pattern<1, 8> {
+template <> struct Pattern<1, 8> : NoTable {
     static constexpr int CK = 64;
     using mask_t = uint64_t;
     struct Sel { uint32_t pa[4], pb[4]; };
@@ -203,6 +280,10 @@ template <> struct Pattern<1, 8> {
             s.pb[q] = msb((bits >> 8) & 0xFFu);
         }
         return s;
+    }
+    __host__ __device__ static __forceinline__ Sel decode_tab(uint64_t m, const uint32_t *)
+    {
+        return decode(m);
     }
     __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &sel, const uint32_t *x,
                                                 float acc)
@@ -223,11 +304,12 @@ template <> struct Pattern<1, 8> {
     }
 };
 
-template <int M> struct DensePattern {  // N == M: every position kept, mask not consulted
+template <int M> struct DensePattern : NoTable {  // N == M: every position kept, mask not consulted
     static constexpr int CK = 8;
     using mask_t = uint8_t;
     struct Sel {};
     __host__ __device__ static __forceinline__ Sel decode(uint32_t) { return Sel{}; }
+    __host__ __device__ static __forceinline__ Sel decode_tab(uint32_t, const uint32_t *) { return Sel{}; }
     __host__ __device__ static __forceinline__ float dot(const uint4 &v, const Sel &, const uint32_t *x,
                                                 float acc)
     {

@@ -99,7 +99,7 @@ struct RowsArgs {
     int seg_v, seg_m;       // shared bytes of one row's value / mask segment
     int stage_bytes;        // R * (seg_v + seg_m)
     int xbuf_bytes;         // one x tile buffer: B * XV * tile_chunks * 16
-    int off_x, off_bar, off_carry;
+    int off_x, off_bar, off_tab, off_carry;
     int y_f32;
     int pair;               // 1: gate/up pair, y = silu(gate x) * (up x) (R == 2)
     int l2pre_rows;         // rows per CTA warmed in L2 before the dependence wait
@@ -182,6 +182,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     uint8_t *xbuf = rows_smem + a.off_x;                                   // [<=2][B][XV][tile]
     uint64_t *full = reinterpret_cast<uint64_t *>(rows_smem + a.off_bar);  // [W][SW]
     float *carry = reinterpret_cast<float *>(rows_smem + a.off_carry);     // [rows of CTA][B]
+    uint32_t *tab = reinterpret_cast<uint32_t *>(rows_smem + a.off_tab);   // [P::kTabWords]
 
     pdl_launch_dependents();
 
@@ -232,6 +233,11 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
         while (issued < a.pre && issued < ntask)
             issue_next(my_ring + static_cast<size_t>(issued) * a.stage_bytes, &my_full[issued]);
 
+    // The mask-decode table (8-wide patterns), published to all warps by the
+    // barrier after the x tile below.
+    if constexpr (P::kTabWords > 0)
+        for (int i = threadIdx.x; i < P::kTabWords; i += blockDim.x) tab[i] = P::tab_entry(i);
+
     // Warm L2 with the CTA's next rows (values and masks of consecutive rows
     // are contiguous) in pieces of up to 32 KB, one piece per lane of the
     // last warp: HBM streams them while the previous kernel drains, and no
@@ -252,6 +258,11 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     }
 
     pdl_wait();  // x may be the previous kernel's output; y may still be read by it
+
+    // loop-invariant strides, read from the parameter block once
+    const int seg_chunks = a.seg_chunks;
+    const int seg_v = a.seg_v, seg_m = a.seg_m;
+    const int xstride = a.tile_chunks * 16;  // bytes between x units (unit-major layout)
 
     bool failed = false;
     int j = 0;          // next task of this warp
@@ -309,7 +320,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                     atomicOr(a.err, kDevErrPipeTimeout);
                 }
                 uint8_t *sv = my_ring + static_cast<size_t>(slot) * a.stage_bytes;
-                const uint8_t *sm = sv + R * a.seg_v;
+                const uint8_t *sm = sv + R * seg_v;
                 // columns [cs, ce) of the K tile; the slot holds them from 0.
                 // All R rows are computed even when the task has nr < R (the
                 // CTA's last row tile): the rows past nr read stale slot
@@ -317,18 +328,23 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                 // address -- and their sums are never stored.  This keeps
                 // the loop free of per-row branches.
                 const int cs = sg * a.seg_chunks;
-                const int ce = min(nc, cs + a.seg_chunks);
-                const uint8_t *xseg = xs + cs * 16;
+                const int ncol = min(nc, cs + seg_chunks) - cs;
+                // per-lane pointers to column `lane` of the segment, advanced
+                // by 32 columns an iteration; the other rows (and x units)
+                // sit at fixed strides from them
+                const uint8_t *vp = sv + lane * 16;
+                const uint8_t *mp = sm + lane * MB;
+                const uint8_t *xp = xs + (cs + lane) * 16;
                 if constexpr (B <= 2) {
 #pragma unroll 2
-                    for (int c = lane; c < ce - cs; c += 32) {
+                    for (int c = lane; c < ncol; c += 32, vp += 512, mp += 32 * MB, xp += 512) {
                         uint32_t xw[B][XR];
 #pragma unroll
                         for (int b = 0; b < B; ++b)
 #pragma unroll
                             for (int u = 0; u < XV; ++u) {
                                 const uint4 t = *reinterpret_cast<const uint4 *>(
-                                    xseg + ((b * XV + u) * a.tile_chunks + c) * 16);
+                                    xp + (b * XV + u) * xstride);
                                 xw[b][4 * u + 0] = t.x;
                                 xw[b][4 * u + 1] = t.y;
                                 xw[b][4 * u + 2] = t.z;
@@ -336,11 +352,9 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                             }
 #pragma unroll
                         for (int i = 0; i < R; ++i) {
-                            const uint4 v =
-                                *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
-                            const mask_t m =
-                                *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB);
-                            const typename P::Sel sel = P::decode(m);
+                            const uint4 v = *reinterpret_cast<const uint4 *>(vp + i * seg_v);
+                            const mask_t m = *reinterpret_cast<const mask_t *>(mp + i * seg_m);
+                            const typename P::Sel sel = P::decode_tab(m, tab);
 #pragma unroll
                             for (int b = 0; b < B; ++b)
                                 acc[i * B + b] = P::dot(v, sel, xw[b], acc[i * B + b]);
@@ -352,14 +366,14 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                     // at most 32 words, in registers at once), each x unit
                     // read once for R rows.
                     constexpr int BG = B < 32 / XR ? B : (32 / XR > 0 ? 32 / XR : 1);
-                    for (int c = lane; c < ce - cs; c += 32) {
+                    for (int c = lane; c < ncol; c += 32, vp += 512, mp += 32 * MB, xp += 512) {
                         uint4 v[R];
                         typename P::Sel sel[R];
 #pragma unroll
                         for (int i = 0; i < R; ++i) {
-                            v[i] = *reinterpret_cast<const uint4 *>(sv + i * a.seg_v + c * 16);
-                            sel[i] = P::decode(
-                                *reinterpret_cast<const mask_t *>(sm + i * a.seg_m + c * MB));
+                            v[i] = *reinterpret_cast<const uint4 *>(vp + i * seg_v);
+                            sel[i] = P::decode_tab(*reinterpret_cast<const mask_t *>(mp + i * seg_m),
+                                                   tab);
                         }
 #pragma unroll
                         for (int b0 = 0; b0 < B; b0 += BG) {
@@ -370,7 +384,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                                 for (int u = 0; u < XV; ++u) {
                                     if (b0 + bb < B) {
                                         const uint4 t = *reinterpret_cast<const uint4 *>(
-                                            xseg + (((b0 + bb) * XV + u) * a.tile_chunks + c) * 16);
+                                            xp + ((b0 + bb) * XV + u) * xstride);
                                         xw[bb][4 * u + 0] = t.x;
                                         xw[bb][4 * u + 1] = t.y;
                                         xw[bb][4 * u + 2] = t.z;
@@ -436,7 +450,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 
 struct RowsPlan {
     int W, R, ktiles, tile_chunks, seg_chunks, nseg, nseg_last, SW, grid;
-    int seg_v, seg_m, stage_bytes, xbuf_bytes, off_x, off_bar, off_carry;
+    int seg_v, seg_m, stage_bytes, xbuf_bytes, off_x, off_bar, off_tab, off_carry;
     size_t smem;
 };
 
@@ -444,11 +458,13 @@ struct RowsPlan {
 // false if nothing fits in shared memory (the caller then takes another
 // kernel).  rows_plan_group does the same for `count` matrices with the same
 // K in one launch and writes each matrix's first CTA to cta_begin[0..count].
-// max_warps caps the warps per CTA.
+// max_warps caps the warps per CTA; tab_bytes is the pattern's shared decode
+// table (Pattern<N, M>::kTabWords words).
 bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
-               RowsPlan *out, bool pair = false);
+               RowsPlan *out, bool pair = false, int tab_bytes = 0);
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
-                     int max_smem, int max_warps, RowsPlan *out, int *cta_begin);
+                     int max_smem, int max_warps, RowsPlan *out, int *cta_begin,
+                     int tab_bytes = 0);
 
 // Shared memory and registers one CTA may take so that two fit on an SM
 // (cached per device); false if the device cannot say.
@@ -525,6 +541,7 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     a.xbuf_bytes = pl.xbuf_bytes;
     a.off_x = pl.off_x;
     a.off_bar = pl.off_bar;
+    a.off_tab = pl.off_tab;
     a.off_carry = pl.off_carry;
     a.y_f32 = p0.y_f32 ? 1 : 0;
 
@@ -622,14 +639,14 @@ cudaError_t launch_rows_pattern(const SpmvGroup &g, cudaStream_t s)
     auto plan = [&](int smem_cap, int max_warps) {
         if (g.count == 1 || g.pair) {
             if (!rows_plan(p0.rows, chunks, P::CK, p0.batch, nsm, smem_cap, max_warps, &pl,
-                           g.pair))
+                           g.pair, 4 * P::kTabWords))
                 return false;
             cta_begin[0] = 0;
             cta_begin[1] = pl.grid;
             return true;
         }
         return rows_plan_group(rows, g.count, chunks, P::CK, p0.batch, nsm, smem_cap, max_warps,
-                               &pl, cta_begin);
+                               &pl, cta_begin, 4 * P::kTabWords);
     };
     // Half an SM per CTA when the plan allows it (the warp cap follows from
     // the chosen instance's registers, allocated 8 a thread at a time);

@@ -8,7 +8,8 @@
 // and x lane p = p + 1: the result must be 1 + the position of the chunk's
 // i-th kept weight, the positions taken group by group in increasing k (the
 // packed layout's fixed-step order).  The dense patterns (N = M) keep every
-// position.
+// position.  Every mask is decoded both from registers alone (decode) and
+// through the shared-memory table of the 8-wide patterns (decode_tab).
 //
 // It also checks the tensor-core product's group expansion (expand_sel in
 // csrc/nm_tc_expand.cuh, used as the two 16-bit selectors the kernel
@@ -51,18 +52,30 @@ void check_mask(uint64_t mask, Result &r)
     uint32_t x[CK / 2];
     for (int w = 0; w < CK / 2; ++w)
         x[w] = f16_of_int(2 * w + 1) | (static_cast<uint32_t>(f16_of_int(2 * w + 2)) << 16);
+    // both decodes: from registers alone, and through the shared-memory
+    // table the streaming kernel builds (word i = tab_entry(i))
+    static uint32_t tab[256];
+    static bool tab_ready = false;
+    if (!tab_ready) {
+        for (int i = 0; i < 256; ++i) tab[i] = P::tab_entry(static_cast<uint32_t>(i));
+        tab_ready = true;
+    }
     const auto sel = P::decode(static_cast<typename P::mask_t>(mask));
+    const auto sel_tab = P::decode_tab(static_cast<typename P::mask_t>(mask), tab);
     for (int i = 0; i < 8; ++i) {
         uint32_t vw[4] = {0, 0, 0, 0};
         vw[i / 2] = static_cast<uint32_t>(0x3C00u) << (16 * (i % 2));
         const uint4 v = make_uint4(vw[0], vw[1], vw[2], vw[3]);
-        const float got = P::dot(v, sel, x, 0.0f);
-        ++r.checks;
-        if (got != static_cast<float>(kept[i] + 1)) {
-            if (r.fails < 5)
-                std::printf("%d:%d mask %016llx slot %d: got %g, want %d\n", N, M,
-                            static_cast<unsigned long long>(mask), i, got, kept[i] + 1);
-            ++r.fails;
+        for (int way = 0; way < 2; ++way) {
+            const float got = P::dot(v, way ? sel_tab : sel, x, 0.0f);
+            ++r.checks;
+            if (got != static_cast<float>(kept[i] + 1)) {
+                if (r.fails < 5)
+                    std::printf("%d:%d mask %016llx slot %d (%s): got %g, want %d\n", N, M,
+                                static_cast<unsigned long long>(mask), i,
+                                way ? "table" : "registers", got, kept[i] + 1);
+                ++r.fails;
+            }
         }
     }
 }
