@@ -44,6 +44,7 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "rows") && (v == 0 || v == 1)) t.rows_kernel = v;
         else if (!std::strcmp(tok, "rows_pair") && (v == 0 || v == 1)) t.rows_pair = v;
         else if (!std::strcmp(tok, "rows_pre") && v >= 0 && v <= 8) t.rows_pre = v;
+        else if (!std::strcmp(tok, "rows_two") && v >= -1 && v <= 1) t.rows_two = v;
         else if (!std::strcmp(tok, "rows_l2pre") && v >= 0) t.rows_l2pre_bytes = v;
         else if (!std::strcmp(tok, "tc") && (v == -1 || v == 0 || v == 1)) t.tc = v;
         else if (!std::strcmp(tok, "tc_lbo") && v >= 0 && v < 16384) t.tc_lbo = v;
@@ -190,14 +191,13 @@ bool bulk_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, B
 
 namespace {
 
-// The row kernel's plan for a K (in chunks), batch and a grid whose busiest
-// CTA has rows_per_cta rows.
-bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, int max_smem,
-                    int max_warps, RowsPlan *out, bool pair = false)
+// The row kernel's plan for a K (in chunks), batch, warp count and a grid
+// whose busiest CTA has rows_per_cta rows.
+bool rows_plan_w(int64_t rows_per_cta, int grid, int chunks, int CK, int B, int max_smem, int W,
+                 RowsPlan *out, bool pair, int tab_bytes)
 {
     const BulkTuning &t = bulk_tuning();
     const int MB = CK / 8;  // mask bytes per chunk
-    const int W = std::min(t.rows_warps ? t.rows_warps : kRowsMaxWarps, max_warps);
     if (W < 1) return false;
 
     // 1. K tile: the x all warps share, B * tile * CK * 2 bytes; all of K
@@ -256,18 +256,21 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
         else if (two_rows) R = R_many;
         else if (t.rows_R) R = p.nseg == 1 ? t.rows_R : 1;
         else if (CK >= 32 && p.nseg == 1) R = 2;  // whole rows: two copies a task
+        else if (CK >= 32 && t.rows_two == 1) R = 2;  // two rows' segments: four copies
         else
             while (p.nseg == 1 && R < 4 && 2 * R * segb <= target && 2 * R * B <= 8) R *= 2;
         if (R > rows_rmax(B)) return false;
         p.R = R;
         p.stage_bytes = R * segb;
 
-        // 3. Shared memory: slots [W][SW] | x buffers | barriers | carry;
-        //    SW from 2 to 4, as many as the ring budget and max_smem allow.
+        // 3. Shared memory: slots [W][SW] | x buffers | barriers | decode
+        //    table | carry; SW from 2 to 4, as many as the ring budget and
+        //    max_smem allow.
+        const int tab = round_up(tab_bytes, 16);
         auto total = [&](int sw) {
             const size_t S = static_cast<size_t>(sw) * W;
             return S * p.stage_bytes + static_cast<size_t>(nxb) * p.xbuf_bytes +
-                   round_up(static_cast<int>(8 * S), 16) + carry;
+                   round_up(static_cast<int>(8 * S), 16) + tab + carry;
         };
         int SW = std::max(2, std::min(4, t.rows_ring_bytes / (W * p.stage_bytes)));
         while (SW > 2 && total(SW) > static_cast<size_t>(max_smem)) --SW;
@@ -276,7 +279,8 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
         p.SW = SW;
         p.off_x = S * p.stage_bytes;
         p.off_bar = p.off_x + nxb * p.xbuf_bytes;
-        p.off_carry = p.off_bar + round_up(8 * S, 16);
+        p.off_tab = p.off_bar + round_up(8 * S, 16);
+        p.off_carry = p.off_tab + tab;
         p.smem = total(SW);
         *out = p;
         return true;
@@ -284,10 +288,49 @@ bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, i
     return false;
 }
 
+// Row tiles are dealt to the warps round robin, so the busiest warp has
+// ceil(tiles / W) of them; the share of warp-time doing work is
+// tiles / (W * ceil(tiles / W)).
+double warp_balance(int64_t rows_per_cta, const RowsPlan &p, bool pair)
+{
+    const int64_t tiles = (rows_per_cta + (pair ? 1 : p.R) - 1) / (pair ? 1 : p.R);
+    if (tiles <= p.W) return 1.0;  // one round: every tile runs at once
+    const int64_t per = (tiles + p.W - 1) / p.W;
+    return static_cast<double>(tiles) / static_cast<double>(per * p.W);
+}
+
+// The plan with the most warps up to max_warps, unless 12 to 15 warps
+// share the CTA's row tiles more evenly (the CTA ends with its busiest
+// warp): e.g. 35 rows take 3 tiles on each of 12 warps instead of 3 on
+// three of 16 and 2 on the rest.  The tuning key rows_warps fixes W.
+bool rows_plan_impl(int64_t rows_per_cta, int grid, int chunks, int CK, int B, int max_smem,
+                    int max_warps, RowsPlan *out, bool pair, int tab_bytes)
+{
+    const BulkTuning &t = bulk_tuning();
+    const int wmax = std::min(t.rows_warps ? t.rows_warps : kRowsMaxWarps, max_warps);
+    RowsPlan best;
+    if (!rows_plan_w(rows_per_cta, grid, chunks, CK, B, max_smem, wmax, &best, pair, tab_bytes))
+        return false;
+    double best_bal = warp_balance(rows_per_cta, best, pair);
+    if (!t.rows_warps)
+        for (int w = wmax - 1; w >= 12; --w) {
+            RowsPlan p;
+            if (!rows_plan_w(rows_per_cta, grid, chunks, CK, B, max_smem, w, &p, pair, tab_bytes))
+                continue;
+            const double bal = warp_balance(rows_per_cta, p, pair);
+            if (bal > best_bal + 0.02) {
+                best = p;
+                best_bal = bal;
+            }
+        }
+    *out = best;
+    return true;
+}
+
 }  // namespace
 
 bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, int max_warps,
-               RowsPlan *out, bool pair)
+               RowsPlan *out, bool pair, int tab_bytes)
 {
     if (rows <= 0 || chunks <= 0 || B < 1 || B > NM_MAX_BATCH) return false;
     const BulkTuning &t = bulk_tuning();
@@ -299,11 +342,11 @@ bool rows_plan(int64_t rows, int chunks, int CK, int B, int nsm, int max_smem, i
     grid = std::max<int64_t>(grid, (rows + max_rows - 1) / max_rows);
     if (grid > 0x7fffffff) return false;
     return rows_plan_impl((rows + grid - 1) / grid, static_cast<int>(grid), chunks, CK, B,
-                          max_smem, max_warps, out, pair);
+                          max_smem, max_warps, out, pair, tab_bytes);
 }
 
 bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, int nsm,
-                     int max_smem, int max_warps, RowsPlan *out, int *cta_begin)
+                     int max_smem, int max_warps, RowsPlan *out, int *cta_begin, int tab_bytes)
 {
     if (count < 1 || count > kRowsMaxGroup || chunks <= 0 || B < 1 || B > NM_MAX_BATCH)
         return false;
@@ -350,7 +393,7 @@ bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, 
         rpc = std::max<int64_t>(rpc, (rows[i] + g[i] - 1) / g[i]);
         cta_begin[i + 1] = cta_begin[i] + g[i];
     }
-    return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, max_warps, out);
+    return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, max_warps, out, false, tab_bytes);
 }
 
 }  // namespace nm

@@ -39,7 +39,7 @@ long g_fail = 0, g_plans = 0, g_none = 0;
     } while (0)
 
 void check_rows_plan(const nm::RowsPlan &p, int64_t rows_per_cta, int chunks, int CK, int B,
-                     const char *what)
+                     const char *what, int tab_bytes)
 {
     const int MB = CK / 8;
     EXPECT(p.smem <= static_cast<size_t>(kMaxSmem), "%s smem %zu", what, p.smem);
@@ -71,8 +71,10 @@ void check_rows_plan(const nm::RowsPlan &p, int64_t rows_per_cta, int chunks, in
     const int S = p.SW * p.W;
     EXPECT(p.off_x == S * p.stage_bytes, "%s off_x", what);
     EXPECT(p.off_bar == p.off_x + (p.ktiles > 1 ? 2 : 1) * p.xbuf_bytes, "%s off_bar", what);
-    EXPECT(p.off_carry >= p.off_bar + 8 * S, "%s off_carry", what);
-    EXPECT(p.off_x % 16 == 0 && p.off_bar % 16 == 0 && p.off_carry % 16 == 0 &&
+    EXPECT(p.off_tab >= p.off_bar + 8 * S, "%s off_tab", what);
+    EXPECT(p.off_carry >= p.off_tab + tab_bytes, "%s off_carry", what);
+    EXPECT(p.off_x % 16 == 0 && p.off_bar % 16 == 0 && p.off_tab % 16 == 0 &&
+               p.off_carry % 16 == 0 &&
                p.stage_bytes % 16 == 0 && p.xbuf_bytes % 16 == 0,
            "%s alignment", what);
     const int64_t carry = p.ktiles > 1 ? rows_per_cta * B * 4 : 0;
@@ -89,13 +91,15 @@ void one(int64_t rows, int64_t K, int N, int M, int B)
     char what[128];
     std::snprintf(what, sizeof(what), "rows %lld K %lld %d:%d B %d", static_cast<long long>(rows),
                   static_cast<long long>(K), N, M, B);
+    // the 8-wide patterns with two or four kept carry a 1 KB decode table
+    const int tab = (M == 8 && (N == 2 || N == 4)) ? 1024 : 0;
     nm::RowsPlan p;
-    if (nm::rows_plan(rows, chunks, CK, B, kNsm, kMaxSmem, nm::kRowsMaxWarps, &p)) {
+    if (nm::rows_plan(rows, chunks, CK, B, kNsm, kMaxSmem, nm::kRowsMaxWarps, &p, false, tab)) {
         ++g_plans;
         EXPECT(p.grid >= 1 && p.grid <= rows, "%s grid %d", what, p.grid);
         const int64_t rpc = (rows + p.grid - 1) / p.grid;
         EXPECT(rpc * p.grid >= rows && (rpc - 1) * p.grid < rows, "%s rpc", what);
-        check_rows_plan(p, rpc, chunks, CK, B, what);
+        check_rows_plan(p, rpc, chunks, CK, B, what, tab);
     } else {
         ++g_none;
         // the chunk-column kernel must then take it
@@ -113,10 +117,11 @@ void group(const std::vector<int64_t> &rows, int64_t K, int N, int M, int B)
     char what[128];
     std::snprintf(what, sizeof(what), "group of %zu, K %lld %d:%d B %d", rows.size(),
                   static_cast<long long>(K), N, M, B);
+    const int tab = (M == 8 && (N == 2 || N == 4)) ? 1024 : 0;
     nm::RowsPlan p;
     int cta_begin[nm::kRowsMaxGroup + 1];
     if (!nm::rows_plan_group(rows.data(), static_cast<int>(rows.size()), chunks, CK, B, kNsm,
-                             kMaxSmem, nm::kRowsMaxWarps, &p, cta_begin)) {
+                             kMaxSmem, nm::kRowsMaxWarps, &p, cta_begin, tab)) {
         ++g_none;
         return;
     }
@@ -132,7 +137,7 @@ void group(const std::vector<int64_t> &rows, int64_t K, int N, int M, int B)
         EXPECT(g >= 1 && g <= rows[i], "%s matrix %zu gets %d CTAs", what, i, g);
         if (g >= 1) rpc = std::max<int64_t>(rpc, (rows[i] + g - 1) / g);
     }
-    check_rows_plan(p, rpc, chunks, CK, B, what);
+    check_rows_plan(p, rpc, chunks, CK, B, what, tab);
 }
 
 }  // namespace
@@ -153,7 +158,10 @@ int main()
         {25600, 25600}, {333, 77, 250, 4, 5, 6, 7, 900}, {1, 1}, {100000, 1}, {700, 300, 1}};
     for (auto &g : groups)
         for (int64_t K : {1024L, 4096L, 5120L, 8192L})
-            for (int B = 1; B <= 8; ++B) group(g, K, 2, 4, B);
+            for (int B = 1; B <= 8; ++B) {
+                group(g, K, 2, 4, B);
+                group(g, K, 4, 8, B);
+            }
     std::printf("%ld plans checked, %ld shapes without a row plan, %ld failures\n", g_plans,
                 g_none, g_fail);
     std::printf(g_fail ? "FAIL\n" : "OK\n");
