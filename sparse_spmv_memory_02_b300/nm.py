@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.nm_select_mask.restype = ctypes.c_int
             L.nm_prune_pack.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp, vp]
             L.nm_prune_pack.restype = ctypes.c_int
+            L.nm_probe_read_stream.argtypes = [vp, sz, vp, vp]
+            L.nm_probe_read_stream.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -329,3 +331,17 @@ def nm_calib_accumulate(X: torch.Tensor, H: torch.Tensor | None = None, stream=N
     ldx = X.stride(0) if T > 1 else K
     _check(lib().nm_calib_accumulate(_ptr(X), T, K, ldx, _ptr(H), H.stride(0), _stream(stream)))
     return H
+
+
+def nm_probe_read_stream(buf: torch.Tensor, sink: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """Read every byte of the contiguous device tensor ``buf`` once (the
+    library's read-only HBM stream, include/nm_probe.h); returns the int32
+    sink holding the XOR of all 32-bit words read."""
+    if not buf.is_contiguous():
+        raise ValueError("buf must be contiguous")
+    if sink is None:
+        sink = torch.empty(1, dtype=torch.int32, device=buf.device)
+    _check(lib().nm_probe_read_stream(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink),
+                                      _stream(stream)))
+    return sink

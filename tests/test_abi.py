@@ -2,6 +2,7 @@
 include/nm.h declares, and rejects bad arguments on the host before any CUDA
 call is made (so these checks need no device)."""
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -13,6 +14,7 @@ from sparse_spmv_memory_02_b300 import nm
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "nm.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -21,9 +23,12 @@ def built():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(nm_[a-z_]+)\s*\(", text)))
+    """Every function any include/*.h declares."""
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(nm_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_interface():
@@ -31,7 +36,16 @@ def test_header_declares_the_interface():
             "nm_spmv_group", "nm_spmv_gate_up_silu", "nm_select_mask", "nm_prune_pack",
             "nm_calib_accumulate",
             "nm_device_errors", "nm_status_str",
-            "nm_last_error", "nm_version"} <= set(declared_functions())
+            "nm_last_error", "nm_version", "nm_pack_noalloc",
+            "nm_probe_read_stream"} <= set(declared_functions())
+
+
+def test_probe_checks_arguments_on_the_host():
+    L = nm.lib()
+    assert L.nm_probe_read_stream(None, 64, 0x1000, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_probe_read_stream(0x1008, 64, 0x1000, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_probe_read_stream(0x1000, 72, 0x1000, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_probe_read_stream(0x1000, 0, 0x1000, None) == nm.NM_OK
 
 
 def test_spmv_group_checks_arguments_on_the_host():
