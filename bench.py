@@ -41,12 +41,9 @@ METRIC = "N:M SpMV µs/call and achieved HBM GB/s (% of peak), batch-1 decode sh
 FALLBACK_HBM_GBS = 6400.0
 
 # DRAM bytes (read + write) per launch, averaged over the launches of one
-# step, from an ncu capture of that step (profiles/); None until captured for
-# the current kernel.
-TRAFFIC_PER_LAUNCH = {
-    # profiles/nm_spmv_rows_llama31_8b_block_2of4_launches.md (12 launches)
-    ("llama31_8b_block", "2:4", 1, "fused"): 61.433e6,
-}
+# step, from an ncu capture of that step taken with the current kernels;
+# workloads without an entry report null.
+TRAFFIC_PER_LAUNCH = {}
 
 
 def parse_args(argv=None):
@@ -72,8 +69,21 @@ def parse_args(argv=None):
     p.add_argument("--no-calib", action="store_true", help="skip the calibration timing")
     p.add_argument("--no-crossover", action="store_true",
                    help="skip the batch crossover against 2:4 sparse tensor cores")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads (single layer, Qwen3-14B MLP pattern sweep, "
+                        "Llama-3.3-70B block at batch 1/2/4/8, 448-layer Qwen3-32B stream)")
     p.add_argument("--calib-tokens", type=int, default=512,
                    help="decode-step tokens per nm_calib_accumulate call in the calibration timing")
+    p.add_argument("--layer", default=None, metavar="ROWSxK",
+                   help="time one product of this shape alone (pattern --pattern, default 2:4; "
+                        "batch --batch) and print one JSON line; the workload options are ignored")
+    p.add_argument("--calls", type=int, default=50, help="--layer: calls per timed sample")
+    p.add_argument("--samples", type=int, default=20, help="--layer: timed samples")
+    p.add_argument("--eager", action="store_true",
+                   help="--layer: launch the calls eagerly instead of from a CUDA graph (for "
+                        "profilers that replay single launches)")
+    p.add_argument("--seed", type=int, default=4242, help="--layer: weight seed (x: seed + 500)")
+    p.add_argument("--batches", default=None, help="--layer: comma-separated batch sizes")
     return p.parse_args(argv)
 
 
@@ -114,7 +124,7 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int, period_ms: int = 50):
+    def __init__(self, index: int, period_ms: int = 20):
         self.index, self.period_ms = index, period_ms
         self.samples, self.proc, self.thread = [], None, None
 
@@ -155,9 +165,8 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, window: str = "timed region"):
         sel = [p for t, p in self.samples if t0 <= t <= t1]
-        window = "timed region"
         if not sel:
             sel = [p for _, p in self.samples]
             window = "whole run (timed region shorter than the sampling period)"
@@ -286,24 +295,31 @@ def capture_step_graphs(layers, copies, fused, silu=False):
     return streams
 
 
-def time_steps(streams, copies, steps, warmup, world):
-    """Replays `steps` steps (rotating over the copies) between CUDA events
-    after `warmup` untimed ones; returns (seconds, wall t0, wall t1)."""
+def time_steps(streams, copies, steps, warmup, world, samples=20):
+    """Replays `steps` steps (rotating over the copies) after `warmup`
+    untimed ones, in `samples` consecutive timed pieces (CUDA events on the
+    replay stream around each piece, no gap between pieces).  Returns
+    (total seconds, per-step seconds of every piece, wall t0, wall t1)."""
     for s in range(warmup):
         streams[s % copies].replay()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    samples = max(1, min(samples, steps))
+    bounds = [round(i * steps / samples) for i in range(samples + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(samples + 1)]
     t_wall0 = time.time()
-    e0.record()
-    for s in range(steps):
-        streams[s % copies].replay()
-    e1.record()
+    ev[0].record()
+    for i in range(samples):
+        for s in range(bounds[i], bounds[i + 1]):
+            streams[s % copies].replay()
+        ev[i + 1].record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world)
-    return e0.elapsed_time(e1) * 1e-3, t_wall0, t_wall1
+    per_step = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 / max(1, bounds[i + 1] - bounds[i])
+                for i in range(samples)]
+    return ev[0].elapsed_time(ev[samples]) * 1e-3, per_step, t_wall0, t_wall1
 
 
 def layer_pass(layers, batch, reps, l2_bytes):
@@ -594,36 +610,203 @@ def dense_pass(layers, copies, steps, warmup):
     return dt, dense_bytes, n
 
 
-def e2e_pass(layers, streams, copies, steps, warmup, batch):
-    """Through the public API with host buffers: per step, pinned-host x ->
-    device (each distinct input vector once), the step's SpMV launches,
-    device y -> pinned host, then the host waits for y (a decode loop needs
-    the result before the next token)."""
-    xs_dev, seen = [], set()
+def e2e_pass(layers, copies, steps, warmup, fused, silu=False):
+    """Through the public API with host buffers.  Every step: all of the
+    step's distinct input vectors are copied from one pinned host buffer into
+    one device buffer, the step's libnm launches run, all of its outputs are
+    copied into one pinned host buffer -- the two copies captured together
+    with the launches in one CUDA graph per weight copy -- and the host waits
+    for the outputs (a decode loop needs them before the next token).
+    Returns (mean seconds per step, per-step seconds, h2d bytes, d2h bytes)."""
+    from sparse_spmv_memory_02_b300.stream import LayerStream
+    srcs = []
     for L in layers:
-        if id(L["x"]) not in seen:
-            seen.add(id(L["x"]))
-            xs_dev.append(L["x"])
-    xs_h = [x.detach().cpu().pin_memory() for x in xs_dev]
-    ys_h = [torch.empty(L["y"].shape, dtype=L["y"].dtype).pin_memory() for L in layers]
-    h2d = sum(t.numel() * t.element_size() for t in xs_h)
-    d2h = sum(t.numel() * t.element_size() for t in ys_h)
+        if not any(L["x"] is t for t in srcs):
+            srcs.append(L["x"])
 
-    def one(s):
-        for xd, xh in zip(xs_dev, xs_h):
-            xd.copy_(xh, non_blocking=True)
-        streams[s % copies].replay()
-        for L, yh in zip(layers, ys_h):
-            yh.copy_(L["y"], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-
-    for s in range(warmup):
-        one(s)
+    def layout(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += -(-t.numel() // 64) * 64  # keep every view 128-byte aligned
+        return offs, n
+    xoff, xn = layout(srcs)
+    youts = [L["y"] for L in layers]
+    yoff, yn = layout(youts)
+    x_dev = torch.zeros(xn, dtype=torch.float16, device="cuda")
+    y_dev = torch.zeros(yn, dtype=youts[0].dtype, device="cuda")
+    x_views = [x_dev[o:o + t.numel()].view(t.shape) for o, t in zip(xoff, srcs)]
+    y_views = [y_dev[o:o + t.numel()].view(t.shape) for o, t in zip(yoff, youts)]
+    for v, t in zip(x_views, srcs):
+        v.copy_(t)
+    x_host = x_dev.cpu().pin_memory()
+    y_host = torch.empty(yn, dtype=y_dev.dtype).pin_memory()
+    xs = [x_views[next(i for i, t in enumerate(srcs) if t is L["x"])] for L in layers]
+    graphs = []
+    for c in range(copies):
+        st = LayerStream([L["mats"][c] for L in layers], xs, y_views, fuse_shared_input=fused,
+                         silu_pairs=silu_pairs(layers) if silu else ())
+        st.run_eager()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                x_dev.copy_(x_host, non_blocking=True)
+                st.run_eager()
+                y_host.copy_(y_dev, non_blocking=True)
+        torch.cuda.current_stream().wait_stream(side)
+        graphs.append(g)
+    cur = torch.cuda.current_stream()
+    for s in range(max(3, warmup)):
+        graphs[s % copies].replay()
+        cur.synchronize()
+    per = []
     t0 = time.perf_counter()
     for s in range(steps):
-        one(s)
+        ts = time.perf_counter()
+        graphs[s % copies].replay()
+        cur.synchronize()
+        per.append(time.perf_counter() - ts)
     dt = (time.perf_counter() - t0) / steps
-    return dt, h2d, d2h
+    h2d = sum(t.numel() * t.element_size() for t in srcs)
+    d2h = sum(t.numel() * t.element_size() for t in youts)
+    del graphs
+    return dt, per, h2d, d2h
+
+
+# ------------------------------------------------------------------ configs
+
+# The workloads every default run reports beside its headline step: the
+# single 1024 x 1024 layer, the Qwen3-14B-shaped MLP at each pattern, the
+# Llama-3.3-70B-shaped block at each batch and the 448-layer Qwen3-32B-shaped
+# stream (the Llama-3.1-8B-shaped block is the headline itself).
+CONFIG_SET = ([("1", "single_1024", "2:4", 1)] +
+              [("3", "qwen3_14b_mlp", p, 1) for p in ("2:4", "4:8", "1:4", "2:8")] +
+              [("4", "llama33_70b_block", "2:4", b) for b in (1, 2, 4, 8)] +
+              [("5", "qwen3_32b_stream", "2:4", 1)])
+NOMINAL_HBM_GBS = 8000.0
+
+
+def graph_of(run_step, nsteps):
+    """One CUDA graph of run_step(0) .. run_step(nsteps - 1)."""
+    for i in range(min(nsteps, 2)):
+        run_step(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(nsteps):
+                run_step(i)
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
+def replay_samples(g, nsteps, samples):
+    """Per-step seconds of `samples` timed replays of a graph of nsteps steps."""
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e-3 / nsteps)
+    return out
+
+
+def config_timing(wl_key, pattern, batch, l2, samples, dense=True):
+    """One workload's decode step: its layers packed, q/k/v and gate/up each
+    one grouped launch, replayed from a CUDA graph of several steps that
+    rotate over enough packed copies (> 3x L2) that every step streams its
+    weights from HBM; and the dense cuBLAS GEMV of the same step."""
+    from sparse_spmv_memory_02_b300.stream import LayerStream
+    wl = nm_synth.WORKLOADS[wl_key]
+    N, M = map(int, pattern.split(":"))
+    comp = sum(layer.rows * (layer.K // M) * N * 2 + layer.rows * layer.K // 8
+               for _, layer in layer_list(wl))
+    copies = int(min(400, max(1, -(-3 * l2 // comp))))
+    layers = build_workload(wl, N, M, batch, copies, keep_dense=dense)
+    step_b = sum(step_bytes(layers, batch))
+    streams = [LayerStream([L["mats"][c] for L in layers], [L["x"] for L in layers],
+                           [L["y"] for L in layers], fuse_shared_input=True)
+               for c in range(copies)]
+    # at least ~50 us of work a replay, and every copy once
+    est = max(comp / 6e12, 2e-6)
+    nsteps = int(max(copies, min(64, -(-50e-6 // est))))
+    g = graph_of(lambda i: streams[i % copies].run_eager(), nsteps)
+    per = replay_samples(g, nsteps, samples)
+    del g
+    p10, med, p90 = percentiles(per)
+    out = {"config": None, "workload": wl_key, "pattern": pattern, "batch": batch,
+           "layers": len(layers), "launches_per_step": streams[0].launches,
+           "copies": copies, "steps_per_sample": nsteps, "samples": len(per),
+           "algorithmic_bytes": step_b, "us_per_step": med * 1e6, "us_p10": p10 * 1e6,
+           "us_p90": p90 * 1e6, "gbs": step_b / med / 1e9}
+    if dense:
+        ys = [torch.empty_like(L["y"]) for L in layers]
+
+        def dense_step(i):
+            c = i % copies
+            for j, L in enumerate(layers):
+                if L["x"].dim() == 1:
+                    torch.mv(L["dense"][c], L["x"], out=ys[j])
+                else:
+                    torch.matmul(L["x"], L["dense"][c].t(), out=ys[j])
+        gd = graph_of(dense_step, nsteps)
+        dper = replay_samples(gd, nsteps, samples)
+        del gd
+        dmed = percentiles(dper)[1]
+        dbytes = sum(L["rows"] * L["K"] * 2 for L in layers)
+        out["dense_us_per_step"] = dmed * 1e6
+        out["dense_gbs"] = dbytes / dmed / 1e9
+        out["speedup_vs_dense"] = dmed / med
+    del layers, streams
+    torch.cuda.empty_cache()
+    return out
+
+
+def read_probe(samples=10, nbytes=8 << 30):
+    """The library's read-only HBM stream over an 8 GiB buffer (> 60x L2):
+    median GB/s of `samples` timed calls."""
+    from sparse_spmv_memory_02_b300 import nm
+    buf = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+    buf.fill_(1)
+    sink = torch.empty(1, dtype=torch.int32, device="cuda")
+    nm.nm_probe_read_stream(buf, sink)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        nm.nm_probe_read_stream(buf, sink)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    del buf
+    torch.cuda.empty_cache()
+    p10, med, p90 = percentiles(ts)
+    return {"gbs": nbytes / med / 1e9, "gbs_p10": nbytes / p90 / 1e9,
+            "gbs_p90": nbytes / p10 / 1e9, "bytes": nbytes, "samples": samples,
+            "kernel": "nm_probe_read_stream (libnm): 16-byte loads, one 1024-thread CTA per SM"}
+
+
+def configs_pass(l2, peak, read_gbs, samples=20, dense=True):
+    out = []
+    for cfg, wl_key, pattern, batch in CONFIG_SET:
+        r = config_timing(wl_key, pattern, batch, l2, samples, dense=dense)
+        r["config"] = cfg
+        r["frac_of_measured_peak"] = r["gbs"] / peak
+        r["frac_of_nominal_8tbs"] = r["gbs"] / NOMINAL_HBM_GBS
+        r["frac_of_read_probe"] = r["gbs"] / read_gbs if read_gbs else None
+        out.append(r)
+    return out
 
 
 # ------------------------------------------------------------------ oracle leg
@@ -772,17 +955,14 @@ def run_ours(args, world, rank, local):
     others = [k for k in variants if k != args.launch]
 
     sampler = ClockSampler(local).start().wait_first() if rank == 0 else None
-    dt, t_wall0, t_wall1 = time_steps(streams, copies, args.steps, args.warmup, world)
+    dt, step_samples, t_wall0, t_wall1 = time_steps(streams, copies, args.steps, args.warmup,
+                                                    world)
     dt = max_over_ranks(dt, world)
     launches = streams[0].launches * args.steps
-    if sampler is not None:
-        sampler.stop()
-        time.sleep(0.5)  # nvidia-smi's shutdown has been seen to stall the GPU briefly
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     # the other launch structures of the same step, same protocol
     other_launch = {}
     for k in others:
-        odt, _, _ = time_steps(variants[k], copies, args.steps, args.warmup, world)
+        odt, _, _, _ = time_steps(variants[k], copies, args.steps, args.warmup, world)
         odt = max_over_ranks(odt, world)
         other_launch[k] = {"launches_per_step": variants[k][0].launches,
                            "us_per_step": odt / args.steps * 1e6,
@@ -791,12 +971,17 @@ def run_ours(args, world, rank, local):
     # end to end right after the device-timed steps, before the other legs
     e2e = None
     if not args.no_e2e:
-        et, h2d, d2h = e2e_pass(layers, streams, copies, max(10, min(args.steps, 500)),
-                                args.warmup, args.batch)
+        et, eper, h2d, d2h = e2e_pass(layers, copies, max(20, min(args.steps, 500)), args.warmup,
+                                      fused=args.launch != "unfused",
+                                      silu=args.launch == "fused_silu")
+        ep10, emed, ep90 = percentiles(eper)
         e2e = {"value": step_b / et / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "us_per_step": et * 1e6,
-               "path": "pinned host x -> device, the step's graph (%s), y -> pinned host, "
-                       "host waits each step" % args.launch}
+               "us_per_step_p10": ep10 * 1e6, "us_per_step_p50": emed * 1e6,
+               "us_per_step_p90": ep90 * 1e6,
+               "path": "one CUDA graph per step: pinned host x -> one device buffer, the "
+                       "step's libnm launches (%s), all y -> one pinned host buffer; the host "
+                       "waits for y every step (wall clock)" % args.launch}
 
     # each layer alone, L2-cold, for the per-layer figures
     l2_bytes = l2
@@ -837,6 +1022,22 @@ def run_ours(args, world, rank, local):
                          "mirrored), bytes H read+write + X"}
         for K, (t, fl, by) in cp.items():
             calib["K%d" % K] = {"us": t * 1e6, "tflops": fl / t / 1e12, "gbs": by / t / 1e9}
+
+    probe = read_probe() if rank == 0 else None
+    peak0, _ = measured_peaks()
+    configs = None
+    if not args.no_configs and rank == 0:
+        configs = configs_pass(l2, peak0, probe["gbs"] if probe else None,
+                               dense=not args.no_dense)
+
+    t_run1 = time.time()
+    if sampler is not None:
+        sampler.stop()
+        time.sleep(0.5)  # nvidia-smi's shutdown has been seen to stall the GPU briefly
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if clocks is not None:
+        clocks["whole_run"] = sampler.summary(t_wall0, t_run1, window="from the headline "
+                                              "timing to the end of the configs leg")
 
     dense = None
     if not args.no_dense:
@@ -884,6 +1085,16 @@ def run_ours(args, world, rank, local):
         calib["tensor_peak_kind"] = tc_kind
     value = world * step_b * args.steps / dt / 1e9
     achieved = step_b * args.steps / dt / 1e9  # this rank's step: all launches are the SpMV kernel
+    sp10, smed, sp90 = percentiles(step_samples)
+    timing = {"samples": len(step_samples), "steps_per_sample": args.steps / len(step_samples),
+              "us_per_step_p10": sp10 * 1e6, "us_per_step_p50": smed * 1e6,
+              "us_per_step_p90": sp90 * 1e6, "gbs_p10": step_b / sp90 / 1e9,
+              "gbs_p50": step_b / smed / 1e9, "gbs_p90": step_b / sp10 / 1e9}
+    peaks = {"measured_copy_gbs": peak, "measured_kind": peak_kind,
+             "nominal_gbs": NOMINAL_HBM_GBS, "read_probe": probe,
+             "frac_of_measured_copy": achieved / peak,
+             "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+             "frac_of_read_probe": achieved / probe["gbs"] if probe else None}
     per_layer = {}
     for L, b, lt in zip(first_block, bytes_per_call, layer_t):
         per_layer[L["name"]] = {"rows": L["rows"], "K": L["K"], "bytes": b, "us": lt * 1e6,
@@ -904,6 +1115,9 @@ def run_ours(args, world, rank, local):
         "calib": calib,
         "crossover": crossover,
         "step_algorithmic_bytes": step_b,
+        "timing": timing,
+        "peaks": peaks,
+        "configs": configs,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,
         "launch": dict({"structure": args.launch, "launches_per_step": streams[0].launches,
@@ -929,11 +1143,108 @@ def run_ours(args, world, rank, local):
     print(json.dumps(out), flush=True)
 
 
+def percentiles(xs):
+    """(p10, median, p90) of a list of samples (nearest rank)."""
+    s = sorted(xs)
+    pick = lambda q: s[min(len(s) - 1, max(0, int(round(q * (len(s) - 1)))))]  # noqa: E731
+    return pick(0.1), statistics.median(s), pick(0.9)
+
+
+def time_samples(run, samples, eager=False):
+    """Seconds of each of `samples` timed runs of `run` (CUDA events on the
+    current stream), replayed from one CUDA graph unless `eager`."""
+    run()
+    torch.cuda.synchronize()
+    g = None
+    if not eager:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                run()
+        torch.cuda.current_stream().wait_stream(side)
+    go = run if eager else g.replay
+    for _ in range(3):
+        go()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        go()
+        e1.record()
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) * 1e-3)
+    del g
+    return out
+
+
+def run_layer(args):
+    """Products of the shapes in --layer (comma-separated ROWSxK), each
+    pattern in --pattern (comma-separated, default 2:4) and each batch in
+    --batches (default --batch), alone: one JSON line each."""
+    from sparse_spmv_memory_02_b300 import build as nmbuild
+    nmbuild.build()
+    batches = [int(b) for b in args.batches.split(",")] if args.batches else [args.batch]
+    for shape in args.layer.split(","):
+        rows, K = (int(v) for v in shape.lower().split("x"))
+        for pat in (args.pattern or "2:4").split(","):
+            N, M = map(int, pat.split(":"))
+            for B in batches:
+                layer_one(args, rows, K, N, M, B)
+
+
+def layer_one(args, rows, K, N, M, B):
+    """One product shape alone: --calls calls a sample rotating over enough
+    packed copies (> 3x L2) that every call streams its weights from HBM."""
+    from sparse_spmv_memory_02_b300 import nm
+    from sparse_spmv_memory_02_b300.stream import algorithmic_bytes
+    W = nm_synth.weights(rows, K, args.seed, "cuda")
+    mask = nm_synth.topn_mask(W, N, M)
+    x = nm_synth.activations(K, B, args.seed + 500, True, "cuda")
+    A = nm.nm_pack(W, mask, N, M)
+    del W, mask
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    ncopy = max(2, -(-3 * l2 // A.nbytes))
+    mats = [A] + [nm.PackedMatrix(A.values.clone(), A.masks.clone(), rows, K, N, M)
+                  for _ in range(ncopy - 1)]
+    y = torch.empty(B, rows, dtype=torch.float16, device="cuda")
+    n = max(args.calls, ncopy)
+
+    def run():
+        for i in range(n):
+            if B == 1:
+                nm.nm_spmv(mats[i % ncopy], x[0], y[0])
+            else:
+                nm.nm_spmv_batched(mats[i % ncopy], x, y)
+    ts = [t / n for t in time_samples(run, args.samples, eager=args.eager)]
+    assert nm.nm_device_errors() == 0
+    p10, med, p90 = percentiles(ts)
+    nbytes = algorithmic_bytes(A, B, 2)
+    peak, peak_kind = measured_peaks()
+    out = {"mode": "layer", "rows": rows, "K": K, "pattern": "%d:%d" % (N, M), "batch": B,
+           "calls_per_sample": n, "samples": len(ts), "copies": ncopy,
+           "launch": "eager" if args.eager else "cuda graph",
+           "us": med * 1e6, "us_p10": p10 * 1e6, "us_p90": p90 * 1e6,
+           "algorithmic_bytes": nbytes, "gbs": nbytes / med / 1e9,
+           "frac_of_peak": nbytes / med / 1e9 / peak, "peak_gbs": peak, "peak_kind": peak_kind,
+           "kernel": _libnm_kernel(rows, B) if (N, M) == (2, 4) and K % 128 == 0 else None}
+    print(json.dumps(out), flush=True)
+    del mats, A, x, y
+    torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_init()
     try:
-        if args.impl == "reference":
+        if args.layer and args.impl == "ours":
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py --layer needs a CUDA GPU")
+            if rank == 0:
+                run_layer(args)
+        elif args.impl == "reference":
             run_reference(args, world, rank)
         else:
             if not torch.cuda.is_available():
