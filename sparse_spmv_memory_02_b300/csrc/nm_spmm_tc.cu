@@ -243,12 +243,22 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
             prefetch_map(&tm_x);
             const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x);
             int issued = 0;
+            // ring positions kept as running counters (no divisions in the
+            // loop): stage s of slab k, and the done[] slot / parity of slab
+            // k - S whose MMAs must have freed stage s
+            int s = 0, qw = 0;
+            uint32_t pw = 0;
             for (int k = 0; k < nslab && !*failed; ++k) {
-                const int s = k % S;
-                if (k >= S && !mbar_wait(&done[(k - S) % Q], ((k - S) / Q) & 1)) {
-                    *failed = 1;
-                    atomicOr(a.err, kDevErrPipeTimeout);
-                    break;
+                if (k >= S) {
+                    if (!mbar_wait(&done[qw], pw)) {
+                        *failed = 1;
+                        atomicOr(a.err, kDevErrPipeTimeout);
+                        break;
+                    }
+                    if (++qw == Q) {
+                        qw = 0;
+                        pw ^= 1u;
+                    }
                 }
                 uint8_t *st = smem + s * a.stage_bytes;
                 // CTAs start at different slabs (the sum is order-free), so
@@ -268,6 +278,7 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
                     tma2d(st + a.off_x + a.x_bytes / 2, &tm_x, ks * kSlabPos + 64, 0, &full[s]);
                 }
                 ++issued;
+                if (++s == S) s = 0;
             }
             for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
                 if (!mbar_wait(&full[k % S], (k / S) & 1)) break;
@@ -286,16 +297,18 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
         const int nkk = ntile == 2 ? 4 : 2;
         const uint32_t dcol = tmem + static_cast<uint32_t>(mi * a.Np);
         if (lane == 0) {
+            int s = 0, d = 0, qd = 0;
+            uint32_t ps = 0, pd = 0;  // parities of full[s] and afull[d]
+            const uint32_t xstage0 = smem_addr(smem + a.off_x);
             for (int k = 0; k < nslab; ++k) {
-                const int s = k % S, d = k % nbuf;
                 if (*failed) break;
-                if (!mbar_spin(&full[s], (k / S) & 1) || !mbar_spin(&afull[d], (k / nbuf) & 1)) {
+                if (!mbar_spin(&full[s], ps) || !mbar_spin(&afull[d], pd)) {
                     *failed = 1;
                     atomicOr(a.err, kDevErrPipeTimeout);
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t xb = smem_addr(smem + s * a.stage_bytes + a.off_x);
+                const uint32_t xb = xstage0 + static_cast<uint32_t>(s * a.stage_bytes);
                 const uint32_t ta = tmem + kAColBase + d * buf_cols + t * 64;
                 for (int kk = kk0; kk < kk0 + nkk; ++kk) {
                     // x: 64-position box kk / 4, 32-byte step kk % 4 inside it
@@ -303,7 +316,16 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
                     mma_ts(dcol, ta + kk * 8, a.desc_hi | ((xb + boff) >> 4), a.idesc,
                            (k > 0 || kk > kk0) ? 1u : 0u);
                 }
-                commit_to(&done[k % Q]);
+                commit_to(&done[qd]);
+                if (++s == S) {
+                    s = 0;
+                    ps ^= 1u;
+                }
+                if (++d == nbuf) {
+                    d = 0;
+                    pd ^= 1u;
+                }
+                if (++qd == Q) qd = 0;
             }
             commit_to(acc);
         }
@@ -319,13 +341,14 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
         const int rr = tile * kTileM + 32 * q + lane;  // row of this lane in the CTA
         const bool warp_live = tile * kTileM + 32 * q < r_count;
         const int rs = rr < r_count ? rr : 0;          // lanes past the rows read row 0
+        const int vc_lo = c_lo >> 1;  // first 16-byte value chunk (16 positions) of the share
+        int s = 0, d = 0, qn = 0;
+        uint32_t ps = 0, pn = 0;  // parities of full[s] and of done[qn] (slab k - nbuf)
         for (int k = 0; k < nslab; ++k) {
-            const int s = k % S, d = k % nbuf;
             // lane 0 polls for the warp
             int ok = 0;
             if (lane == 0)
-                ok = !*failed && mbar_spin(&full[s], (k / S) & 1) &&
-                     (k < nbuf || mbar_spin(&done[(k - nbuf) % Q], ((k - nbuf) / Q) & 1));
+                ok = !*failed && mbar_spin(&full[s], ps) && (k < nbuf || mbar_spin(&done[qn], pn));
             ok = __shfl_sync(0xffffffffu, ok, 0);
             __syncwarp();
             if (!ok) {
@@ -334,6 +357,10 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
                     atomicOr(a.err, kDevErrPipeTimeout);
                 }
                 break;
+            }
+            if (k >= nbuf && ++qn == Q) {
+                qn = 0;
+                pn ^= 1u;
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (warp_live) {
@@ -345,25 +372,25 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAColBase +
                                     d * buf_cols + tile * 64 + c_lo * 4;
                 for (int g4 = 0; g4 < nc4; ++g4) {
-                    // four chunks = 32 positions = one mask word
+                    // 32 positions = one mask word = two 16-byte value chunks
                     const int g = (c_lo >> 2) + g4;
                     const uint32_t mword = g == 0 ? m4.x : g == 1 ? m4.y : g == 2 ? m4.z : m4.w;
                     uint32_t w[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        // dense chunk c: positions 8c .. 8c+7 = groups 2c, 2c+1
-                        // (value words 2c and 2c+1 of the row)
-                        const int c = c_lo + 4 * g4 + j;
-                        const uint4 vv = *reinterpret_cast<const uint4 *>(
-                            vrow + (((c >> 1) ^ (rs & 7)) << 4));
-                        const uint32_t v0 = (c & 1) ? vv.z : vv.x;
-                        const uint32_t v1 = (c & 1) ? vv.w : vv.y;
-                        const uint32_t bits = mword >> (8 * j);
-                        const uint2 s0 = sel_tab[bits & 15u], s1 = sel_tab[(bits >> 4) & 15u];
-                        w[4 * j + 0] = prmt(v0, 0u, s0.x);
-                        w[4 * j + 1] = prmt(v0, 0u, s0.y);
-                        w[4 * j + 2] = prmt(v1, 0u, s1.x);
-                        w[4 * j + 3] = prmt(v1, 0u, s1.y);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        // value chunk vc: groups 4 vc .. 4 vc + 3, one value
+                        // pair (word) each, loaded once
+                        const int vc = vc_lo + 2 * g4 + h2;
+                        const uint4 vv =
+                            *reinterpret_cast<const uint4 *>(vrow + ((vc ^ (rs & 7)) << 4));
+                        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            // group 4 h2 + qq of the word: its two dense words
+                            const uint2 e = sel_tab[(mword >> (16 * h2 + 4 * qq)) & 15u];
+                            w[8 * h2 + 2 * qq] = prmt(vw[qq], 0u, e.x);
+                            w[8 * h2 + 2 * qq + 1] = prmt(vw[qq], 0u, e.y);
+                        }
                     }
                     tmem_st16(ta + 16 * g4, w);
                 }
@@ -372,6 +399,11 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[d]);
+            if (++s == S) {
+                s = 0;
+                ps ^= 1u;
+            }
+            if (++d == nbuf) d = 0;
         }
     }
 
