@@ -313,7 +313,9 @@ nm_status nm_spmv_gate_up_silu(const nm_matrix *gate, const nm_matrix *up, const
  * product sets NM_DEVERR_SMEM_ALIGN, and writes nothing, if its dynamic
  * shared memory does not start on a 1024-byte boundary (its swizzled copies
  * need that; CUDA places it there).  Synchronises `stream` (so it cannot be
- * captured in a CUDA graph).
+ * captured in a CUDA graph).  A test aid exercises the time-out path without
+ * a fault: with NM_BULK_TUNE=wait_fault_test=1 in the environment the
+ * streaming SpMV kernel issues no copies and gives up its waits after 2 ms.
  * Errors: NM_ERR_INVALID_ARG (flags NULL, capturing stream), NM_ERR_CUDA.
  */
 #define NM_DEVERR_PIPE_TIMEOUT 1u

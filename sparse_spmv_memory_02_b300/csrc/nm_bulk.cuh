@@ -275,12 +275,16 @@ struct BulkTuning {
     int tc = -1;                   // 1: wherever it applies, 0: never, -1: batch 8 with
                                    // more than 128 rows a CTA (two MMA tiles)
     int tc_lbo = 1;                // encoded leading-byte-offset field of its descriptors
+    // Test of the device-side failure path only: the row kernel issues no
+    // copies and waits 2 ms (not 2 s) on its slot barriers, so every wait
+    // runs out, the error word is set and the kernel returns.
+    int wait_fault_test = 0;
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows_two, rows (row-per-warp kernel),
-// ctas, pdl
+// ctas, pdl, wait_fault_test
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 

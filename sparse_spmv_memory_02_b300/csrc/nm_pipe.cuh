@@ -74,14 +74,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false if it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// false if it has not completed within limit_ns (default kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 7u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 7u) == 0 && global_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -103,6 +103,9 @@ struct RowsArgs {
     int y_f32;
     int pair;               // 1: gate/up pair, y = silu(gate x) * (up x) (R == 2)
     int l2pre_rows;         // rows per CTA warmed in L2 before the dependence wait
+    int no_copy;            // test of the wait time-out: issue no copies (nothing ever
+                            // completes a slot barrier, nothing is in flight at exit)
+    uint64_t wait_limit_ns; // limit of every slot-barrier wait
     int cta_begin[kRowsMaxGroup + 1];  // first CTA of each matrix; [nmat] = grid
     int64_t ldx, vrow_bytes, mrow_bytes;
     unsigned int *err;      // device error word
@@ -114,6 +117,23 @@ constexpr int kRowsMaxWarps = 16;
 // Largest rows per task a batch size is built for (R * B partial sums per
 // lane: at most 8 for one or two vectors, 16 from three up).
 __host__ __device__ constexpr int rows_rmax(int B) { return B <= 2 ? 4 : 2; }
+
+// Layout of the x tile in shared memory, in 16-byte units (XV = CK / 8 units
+// per chunk column and vector).  One or two vectors: unit-major, unit u of
+// vector b for column c at (b * XV + u) * tile + c, so that a warp reading
+// one unit of 32 consecutive columns reads 512 contiguous bytes.  Three or
+// more: column-major, column c's B * XV units contiguous and padded to an
+// odd count (rows_x_col_units), so a lane reaches every unit of its column
+// at a compile-time offset, and 8 lanes on consecutive columns (an odd
+// number of units apart) hit 8 different 16-byte bank groups.
+__host__ __device__ constexpr int rows_x_col_units(int B, int CK)
+{
+    return B <= 2 ? 0 : ((B * (CK / 8)) % 2 == 0 ? B * (CK / 8) + 1 : B * (CK / 8));
+}
+__host__ __device__ constexpr int rows_x_tile_bytes(int B, int CK, int tile_chunks)
+{
+    return B <= 2 ? B * (CK / 8) * tile_chunks * 16 : rows_x_col_units(B, CK) * tile_chunks * 16;
+}
 
 // Copies task (K tile kt, segment sg, rows i0 .. i0+nr-1 of the CTA) into a
 // slot: the rows' value segments at st + i * seg_v, their mask segments at
@@ -173,6 +193,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     constexpr int MB = CK / 8;  // mask bytes per chunk
     constexpr int V = pow2_ceil(R * B);
     constexpr int SH = 5 - log2i<V>();
+    constexpr int XCU = rows_x_col_units(B, CK);  // x units a column (0: unit-major)
 
     extern __shared__ __align__(128) uint8_t rows_smem[];
     const int W = blockDim.x >> 5;
@@ -197,6 +218,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     const int nrt = (r_count + RT - 1) / RT;                       // row tiles of the CTA
     const int per_kt = nrt > warp ? (nrt - warp + W - 1) / W : 0;  // this warp's tiles per K tile
     const int ntask = per_kt * ((a.ktiles - 1) * a.nseg + a.nseg_last);
+    const int ncopy = a.no_copy ? 0 : ntask;  // tasks whose copies are issued
     uint8_t *my_ring = ring + static_cast<size_t>(warp) * a.SW * a.stage_bytes;
     uint64_t *my_full = full + warp * a.SW;
     const uint64_t pol = l2_evict_first_policy();
@@ -230,7 +252,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
     // This warp's first `pre` tasks (weights only: no dependence on the
     // previous kernel); the rest of its first SW after x is staged.
     if (lane == 0)
-        while (issued < a.pre && issued < ntask)
+        while (issued < a.pre && issued < ncopy)
             issue_next(my_ring + static_cast<size_t>(issued) * a.stage_bytes, &my_full[issued]);
 
     // The mask-decode table (8-wide patterns), published to all warps by the
@@ -273,11 +295,9 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
         const int nc = min(a.tile_chunks, a.chunks - c0);
         const int nseg = kt == a.ktiles - 1 ? a.nseg_last : a.nseg;
         uint8_t *xs = xbuf + (kt & 1) * a.xbuf_bytes;
-        // x tile -> shared memory, unit-major: unit u of chunk column c of
-        // vector b at ((b * XV + u) * tile_chunks + c) * 16, so that a warp
-        // reading one unit of 32 consecutive columns reads 512 contiguous
-        // bytes.  The buffer written here was last read in K tile kt-2, and
-        // every warp has passed the barrier of tile kt-1 since.
+        // x tile -> shared memory in the layout of rows_x_col_units.  The
+        // buffer written here was last read in K tile kt-2, and every warp
+        // has passed the barrier of tile kt-1 since.
         // Each thread issues up to XU loads before its first store, so a
         // tile costs one memory round trip per XU * blockDim units.
         constexpr int XU = 4;
@@ -293,7 +313,8 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                     const int r = e - b * (XV * nc);
                     const int c = r / XV, u = r - (r / XV) * XV;
                     t[q] = ld_cg_v4(mt.x + b * a.ldx + static_cast<int64_t>(c0 + c) * CK + 8 * u);
-                    dst[q] = ((b * XV + u) * a.tile_chunks + c) * 16;
+                    dst[q] = XCU == 0 ? ((b * XV + u) * a.tile_chunks + c) * 16
+                                      : (c * XCU + b * XV + u) * 16;
                 }
             }
 #pragma unroll
@@ -302,7 +323,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                     *reinterpret_cast<uint4 *>(xs + dst[q]) = t[q];
         }
         if (kt == 0 && lane == 0)
-            while (issued < a.SW && issued < ntask)
+            while (issued < a.SW && issued < ncopy)
                 issue_next(my_ring + static_cast<size_t>(issued) * a.stage_bytes,
                            &my_full[issued]);
         named_barrier_sync(1, blockDim.x);
@@ -315,7 +336,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 #pragma unroll
             for (int t = 0; t < V; ++t) acc[t] = 0.f;
             for (int sg = 0; sg < nseg; ++sg, ++j) {
-                if (!failed && !mbar_wait(&my_full[slot], phase)) {
+                if (!failed && !mbar_wait(&my_full[slot], phase, a.wait_limit_ns)) {
                     failed = true;  // give up waiting; y is garbage, the error word says so
                     atomicOr(a.err, kDevErrPipeTimeout);
                 }
@@ -366,7 +387,9 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                     // at most 32 words, in registers at once), each x unit
                     // read once for R rows.
                     constexpr int BG = B < 32 / XR ? B : (32 / XR > 0 ? 32 / XR : 1);
-                    for (int c = lane; c < ncol; c += 32, vp += 512, mp += 32 * MB, xp += 512) {
+                    const uint8_t *xq = xs + (cs + lane) * (XCU * 16);  // column-major x
+                    for (int c = lane; c < ncol;
+                         c += 32, vp += 512, mp += 32 * MB, xq += 32 * XCU * 16) {
                         uint4 v[R];
                         typename P::Sel sel[R];
 #pragma unroll
@@ -384,7 +407,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                                 for (int u = 0; u < XV; ++u) {
                                     if (b0 + bb < B) {
                                         const uint4 t = *reinterpret_cast<const uint4 *>(
-                                            xp + ((b0 + bb) * XV + u) * xstride);
+                                            xq + ((b0 + bb) * XV + u) * 16);
                                         xw[bb][4 * u + 0] = t.x;
                                         xw[bb][4 * u + 1] = t.y;
                                         xw[bb][4 * u + 2] = t.z;
@@ -405,7 +428,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
                 // task SW ahead (generic-proxy reads, then async-proxy
                 // writes of the same bytes: fence between them).
                 __syncwarp();
-                if (lane == 0 && issued < ntask && !failed) {
+                if (lane == 0 && issued < ncopy && !failed) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     issue_next(sv, &my_full[slot]);
                 }
@@ -544,6 +567,10 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     a.off_tab = pl.off_tab;
     a.off_carry = pl.off_carry;
     a.y_f32 = p0.y_f32 ? 1 : 0;
+    // the time-out test: no copies, and a 2 ms limit on the waits that then
+    // cannot complete
+    a.no_copy = bulk_tuning().wait_fault_test ? 1 : 0;
+    a.wait_limit_ns = bulk_tuning().wait_fault_test ? 2000000ull : kWaitLimitNs;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cta_begin[nmat]);

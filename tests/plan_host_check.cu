@@ -65,8 +65,13 @@ void check_rows_plan(const nm::RowsPlan &p, int64_t rows_per_cta, int chunks, in
            "%s seg_m %d", what, p.seg_m);
     EXPECT(p.stage_bytes == p.R * (p.seg_v + p.seg_m), "%s stage", what);
     EXPECT(p.R >= 1 && p.R <= nm::rows_rmax(B) && p.R * B <= 16, "%s R %d B %d", what, p.R, B);
-    // x buffer: B vectors of the tile's positions, fp16
-    EXPECT(p.xbuf_bytes == B * p.tile_chunks * CK * 2, "%s xbuf", what);
+    // x buffer: B vectors of the tile's positions, fp16; from three vectors
+    // each column's units padded to an odd count
+    const int col_units = B <= 2 ? 0 : B * (CK / 8) + ((B * (CK / 8)) % 2 == 0 ? 1 : 0);
+    EXPECT(p.xbuf_bytes == (B <= 2 ? B * p.tile_chunks * CK * 2 : col_units * p.tile_chunks * 16),
+           "%s xbuf", what);
+    EXPECT(col_units == nm::rows_x_col_units(B, CK) && (B <= 2 || col_units % 2 == 1),
+           "%s column units", what);
     // regions in order, 16-byte aligned, inside smem
     const int S = p.SW * p.W;
     EXPECT(p.off_x == S * p.stage_bytes, "%s off_x", what);
