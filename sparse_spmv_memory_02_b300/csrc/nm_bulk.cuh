@@ -279,12 +279,17 @@ struct BulkTuning {
     // copies and waits 2 ms (not 2 s) on its slot barriers, so every wait
     // runs out, the error word is set and the kernel returns.
     int wait_fault_test = 0;
+    int tc_sp = 0;                 // 1: the tensor-core product takes the packed values as the
+                                   // sparse A operand (tcgen05.mma.sp) instead of expanding them
+    int sp_meta = 0;               // metadata nibble order of that path (0: i0 | i1 << 2)
+    int sp_acc = 2;                // accumulator sets each MMA issuer of that path rotates over
+    int sp_mbufs = 0;              // its metadata buffers (0: as many as tensor memory holds)
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows_two, rows (row-per-warp kernel),
-// ctas, pdl, wait_fault_test
+// ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 

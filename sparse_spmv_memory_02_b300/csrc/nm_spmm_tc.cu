@@ -41,6 +41,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "nm_bulk.cuh"  // bulk_tuning()
 #include "nm_device.cuh"
 #include "nm_internal.h"
 #include "nm_pipe.cuh"
@@ -454,6 +455,348 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
     }
 }
 
+// ------------------------------------------------------------------------
+// The same product with the packed values as the sparse A operand of
+// tcgen05.mma.sp: the 2:4 layout already is the compressed matrix the sparse
+// tensor cores take (two values a group of four, in increasing k), so
+// nothing is expanded.  Per 128-position slab:
+//   * warps 8-10 (lane 0) copy by TMA the CTA's values ({64 values, rows}
+//     box, 128-byte swizzle: the K-major A operand as it lands), its mask
+//     words and x (as in the kernel above), one warp each;
+//   * warps 0-7 (warp w: tile w / 4, rows 32 (w % 4) ..) turn each row's four
+//     mask words into four metadata words (sp_meta_word: one per MMA of 32
+//     positions) and store them into tensor memory, rows r and r + 8 of each
+//     16-row block sharing lanes r and r + 8 (sp_meta_lane_word).  That layout
+//     was read off the GPU: with one-hot x and w = position + 1, the product
+//     shows which kept value each row multiplies with each x position, and
+//     for all 4096 groups of a 128 x 128 slab with random masks it matched
+//     this interleave exactly (one column per MMA, lane = row, placed
+//     group g of every row at the lane and nibble predicted for only half of
+//     them);
+//   * warps 11-14 (lane 0) issue tcgen05.mma.sp (M = 128, N = batch padded to
+//     16 or 32, K = 32 positions = 16 values, fp32 accumulators), each into
+//     its own accumulator columns, and commit once a slab;
+//   * warps 0-7 read the accumulators, add the issuers' partial sums and
+//     round into y.
+constexpr int kSpConvWarps = 8;
+constexpr int kSpProdWarp = 8;        // warps 8-10: producers
+constexpr int kSpProdWarps = 3;
+constexpr int kSpMmaWarps = 4;        // warps 11-14: MMA issuers
+constexpr int kSpThreads = 32 * (kSpConvWarps + kSpProdWarps + kSpMmaWarps);
+constexpr int kSpMaxStages = 32;      // ring stages (a stage holds only the rows it loads)
+constexpr int kSpMaxMetaBufs = 12;    // metadata buffers (ntile x 4 MMAs each)
+constexpr int kSpMaxAccSets = 4;      // accumulator sets an issuer rotates over, slab by slab
+constexpr uint32_t kSpTmemCols = 512; // accumulators first, then metadata
+// Tensor memory: issuer i's accumulator set j at column (i * nacc + j) * Np
+// (4 issuers); from meta_base, each MMA's metadata word in its own column,
+// 8-column aligned: meta_base + 8 * ((d * ntile + t) * 4 + kk) for buffer d,
+// tile t, MMA kk.
+__host__ __device__ constexpr uint32_t sp_meta_col(uint32_t meta_base, int ntile, int d, int t,
+                                                   int kk)
+{
+    return meta_base + 8u * static_cast<uint32_t>((d * ntile + t) * 4 + kk);
+}
+
+struct SpArgs {
+    void *y;
+    int64_t ldy;
+    int rows, K, batch, Np;
+    int row_base, row_extra;
+    int y_f32;
+    uint32_t idesc;           // tcgen05 instruction descriptor, sparse bit set
+    uint64_t desc_hi;         // K-major, 128-byte swizzle, SBO 1024 (A and B)
+    int ntile;                // 128-row MMA tiles a CTA (1 or 2)
+    int S;                    // ring stages
+    int off_m, off_x;         // masks and x inside a stage (values at 0, ntile * 16 KB)
+    int stage_bytes, x_bytes, off_bar;
+    int x3d;
+    int meta_mode;            // sp_meta_word mode
+    int nacc;                 // accumulator sets per issuer (independent chains of MMAs)
+    int nmbuf;                // metadata buffers in tensor memory
+    uint32_t meta_base;       // first metadata column (after 4 * nacc * Np accumulators)
+    unsigned int *err;
+};
+
+// D[tmem_d] (+)= A[a_desc] * B[b_desc], A 2:4-sparse with metadata at tmem_e.
+__device__ __forceinline__ void mma_sp_ss(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t tmem_e, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.sp.cta_group::1.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}" ::"r"(tmem_d),
+        "l"(a_desc), "l"(b_desc), "r"(tmem_e), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// One 32-bit column into this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r0)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r0)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kSpThreads, 1)
+nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
+                  const __grid_constant__ CUtensorMap tm_masks,
+                  const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ SpArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t sp_smem_raw[];
+    uint8_t *smem = sp_smem_raw;
+    // every operand region starts 1024-byte aligned (swizzled boxes, MMA
+    // descriptors) and the metadata columns fit the allocation: else nothing
+    if (((smem_addr(sp_smem_raw) | a.stage_bytes | a.off_m | a.off_x) & 1023u) ||
+        a.S < 2 || a.S > kSpMaxStages ||
+        a.nmbuf < 1 || a.nmbuf > kSpMaxMetaBufs || a.nacc < 1 || a.nacc > kSpMaxAccSets ||
+        a.meta_base < static_cast<uint32_t>(4 * a.nacc * a.Np) ||
+        sp_meta_col(a.meta_base, a.ntile, a.nmbuf - 1, a.ntile - 1, 3) >= kSpTmemCols) {
+        if (threadIdx.x == 0) atomicOr(a.err, kDevErrSmemAlign);
+        return;
+    }
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + a.off_bar);
+    // a stage's three copies complete on their own barriers: values and x
+    // (-> MMA), mask words (-> metadata warps)
+    uint64_t *fullv = bars;                      // [S]
+    uint64_t *fullm = fullv + kSpMaxStages;      // [S]
+    uint64_t *fullx = fullm + kSpMaxStages;      // [S]
+    uint64_t *done = fullx + kSpMaxStages;       // [Q] MMA -> producers, metadata warps
+    uint64_t *mfull = done + kSpMaxStages + 1;   // [nmbuf] metadata warps -> MMA
+    uint64_t *acc = mfull + kSpMaxMetaBufs;      // MMA -> epilogue
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc + 1);
+    volatile int *failed = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int r_begin = cta * a.row_base + min(cta, a.row_extra);
+    const int r_count = a.row_base + (cta < a.row_extra ? 1 : 0);
+    const int ntile = (r_count + kTileM - 1) / kTileM;  // this CTA's tiles (<= a.ntile)
+    const int nconv = 4 * ntile;                        // metadata warps at work
+    const int nslab = a.K / kSlabPos;
+    const int S = a.S;
+    const int NB = a.nmbuf;
+    const int Q = max(S, NB) + 1;  // exceeds both ring depths
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&fullv[s], 1);
+            mbar_init(&fullm[s], 1);
+            mbar_init(&fullx[s], 1);
+        }
+        for (int j = 0; j < Q; ++j) mbar_init(&done[j], kSpMmaWarps);  // one commit an issuer
+        for (int d = 0; d < NB; ++d) mbar_init(&mfull[d], nconv);
+        mbar_init(acc, kSpMmaWarps);
+        *failed = 0;
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(tmem_slot)),
+                     "r"(kSpTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= kSpProdWarp && warp < kSpProdWarp + kSpProdWarps) {
+        // ------------------------------------------------ TMA producers
+        // Three warps, one copy each a slab (values, mask words, x): issuing a
+        // tensor copy blocks the issuing thread for a while, and the three
+        // issue in parallel.  Each arrives on the stage's barrier with its
+        // own byte count on its own barrier.
+        const int role = warp - kSpProdWarp;
+        uint64_t *full = role == 0 ? fullv : role == 1 ? fullm : fullx;
+        if (lane == 0) {
+            const CUtensorMap *map = role == 0 ? &tm_vals : role == 1 ? &tm_masks : &tm_x;
+            prefetch_map(map);
+            const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x);
+            const uint32_t box_rows = static_cast<uint32_t>(a.row_base + (a.row_extra ? 1 : 0));
+            const uint32_t tx = role == 0 ? box_rows * 128u
+                              : role == 1 ? box_rows * 16u
+                                          : static_cast<uint32_t>(a.x_bytes);
+            int issued = 0, s = 0, qw = 0;
+            uint32_t pw = 0;
+            for (int k = 0; k < nslab && !*failed; ++k) {
+                if (k >= S) {
+                    if (!mbar_wait(&done[qw], pw)) {
+                        *failed = 1;
+                        atomicOr(a.err, kDevErrPipeTimeout);
+                        break;
+                    }
+                    if (++qw == Q) {
+                        qw = 0;
+                        pw ^= 1u;
+                    }
+                }
+                uint8_t *st = smem + s * a.stage_bytes;
+                int ks = k + slab0;
+                if (ks >= nslab) ks -= nslab;
+                mbar_arrive_expect_tx(&full[s], tx);
+                if (role == 0) {
+                    tma2d(st, &tm_vals, ks * 64, r_begin, &full[s]);
+                } else if (role == 1) {
+                    tma2d(st + a.off_m, &tm_masks, ks * 4, r_begin, &full[s]);
+                } else if (a.x3d) {
+                    tma3d(st + a.off_x, &tm_x, 0, 0, 2 * ks, &full[s]);
+                } else {
+                    tma2d(st + a.off_x, &tm_x, ks * kSlabPos, 0, &full[s]);
+                    tma2d(st + a.off_x + a.x_bytes / 2, &tm_x, ks * kSlabPos + 64, 0, &full[s]);
+                }
+                ++issued;
+                if (++s == S) s = 0;
+            }
+            // before the CTA can exit, every copy this thread issued must have
+            // landed
+            for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
+                if (!mbar_wait(&full[k % S], (k / S) & 1)) break;
+        }
+    } else if (warp >= kSpProdWarp + kSpProdWarps) {
+        // ------------------------------------------------ MMA issuers
+        // Issuer i: with two tiles, tile i / 2 and MMAs 2 (i % 2), +1 of the
+        // slab; with one tile, MMA i.  Each accumulates into its own sets.
+        const int mi = warp - kSpProdWarp - kSpProdWarps;
+        const int t = ntile == 2 ? (mi >> 1) : 0;
+        const int kk0 = ntile == 2 ? 2 * (mi & 1) : mi;
+        const int nkk = ntile == 2 ? 2 : 1;
+        const uint32_t dcol0 = tmem + static_cast<uint32_t>(mi * a.nacc * a.Np);
+        if (lane == 0) {
+            int s = 0, d = 0, qd = 0, ka = 0;  // ka: accumulator set of slab k
+            uint32_t ps = 0, pd = 0;
+            const uint32_t stage0 = smem_addr(smem);
+            for (int k = 0; k < nslab; ++k) {
+                if (*failed) break;
+                if (!mbar_spin(&fullv[s], ps) || !mbar_spin(&fullx[s], ps) ||
+                    !mbar_spin(&mfull[d], pd)) {
+                    *failed = 1;
+                    atomicOr(a.err, kDevErrPipeTimeout);
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t st = stage0 + static_cast<uint32_t>(s * a.stage_bytes);
+                const uint32_t av = st + static_cast<uint32_t>(t) * (kTileM * 128u);
+                const uint32_t xb = st + static_cast<uint32_t>(a.off_x);
+                for (int kk = kk0; kk < kk0 + nkk; ++kk) {
+                    // A: 16 values (32 bytes) of each row from value 16 kk of
+                    // the slab; x: 32 positions, box kk / 2, 64-byte step kk % 2
+                    const uint32_t aoff = static_cast<uint32_t>(kk) * 32u;
+                    const uint32_t boff = (kk >> 1) * (a.x_bytes / 2) + (kk & 1) * 64;
+                    const uint32_t meta = tmem + sp_meta_col(a.meta_base, a.ntile, d, t, kk);
+                    // slab k adds into set k % nacc: the first slab of each set
+                    // starts it
+                    mma_sp_ss(dcol0 + static_cast<uint32_t>(ka * a.Np),
+                              a.desc_hi | ((av + aoff) >> 4), a.desc_hi | ((xb + boff) >> 4),
+                              meta, a.idesc, (k >= a.nacc || kk > kk0) ? 1u : 0u);
+                }
+                commit_to(&done[qd]);
+                if (++s == S) {
+                    s = 0;
+                    ps ^= 1u;
+                }
+                if (++d == NB) {
+                    d = 0;
+                    pd ^= 1u;
+                }
+                if (++qd == Q) qd = 0;
+                if (++ka == a.nacc) ka = 0;
+            }
+            commit_to(acc);
+        }
+    } else if (warp < nconv) {
+        // ------------------------------------------------ metadata (warps 0-7)
+        const int t = warp >> 2, q = warp & 3;
+        const int rr = t * kTileM + 32 * q + lane;     // row of this lane in the CTA
+        const int rs = rr < r_count ? rr : 0;          // lanes past the rows read row 0
+        const uint32_t tlanes = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        int s = 0, d = 0, qn = 0;
+        uint32_t ps = 0, pn = 0;
+        for (int k = 0; k < nslab; ++k) {
+            int ok = 0;
+            if (lane == 0)
+                ok = !*failed && mbar_spin(&fullm[s], ps) &&
+                     (k < NB || mbar_spin(&done[qn], pn));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0 && !*failed) {
+                    *failed = 1;
+                    atomicOr(a.err, kDevErrPipeTimeout);
+                }
+                break;
+            }
+            if (k >= NB && ++qn == Q) {
+                qn = 0;
+                pn ^= 1u;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint4 m4 =
+                *reinterpret_cast<const uint4 *>(smem + s * a.stage_bytes + a.off_m + rs * 16);
+            const uint32_t mw[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                // this row's metadata word for MMA kk, interleaved with that of
+                // the row 8 apart (sp_meta_lane_word)
+                const uint32_t own = sp_meta_word(mw[kk], a.meta_mode);
+                const uint32_t partner = __shfl_xor_sync(0xffffffffu, own, 8);
+                tmem_st1(tlanes + sp_meta_col(a.meta_base, a.ntile, d, t, kk),
+                         sp_meta_lane_word(own, partner, (lane & 8) != 0));
+            }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mfull[d]);
+            if (++s == S) {
+                s = 0;
+                ps ^= 1u;
+            }
+            if (++d == NB) d = 0;
+        }
+    }
+
+    // ---------------------------------------------------- epilogue
+    __syncwarp();
+    bool ok = true;
+    if (warp < nconv) ok = __all_sync(0xffffffffu, mbar_wait(acc, 0)) != 0;
+    if (!ok && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
+    const bool go = __syncthreads_and(ok && *failed == 0) != 0;
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (go && warp < nconv) {
+        const int t = warp >> 2, q = warp & 3;
+        const int row = t * kTileM + 32 * q + lane;
+        // the tile's partial sums: every accumulator set of issuers 2t, 2t + 1
+        // (two tiles) or 0-3 (sets used: min(nacc, nslab))
+        const int p0 = (ntile == 2 ? 2 * t : 0) * a.nacc;
+        const int np = (ntile == 2 ? 2 : 4) * a.nacc;
+        const int nused = min(a.nacc, nslab);
+        const uint32_t lanes = static_cast<uint32_t>(32 * q) << 16;
+        for (int b0 = 0; b0 < a.Np; b0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + lanes + p0 * a.Np + b0, v);
+            for (int pi = 1; pi < np; ++pi) {
+                if (pi % a.nacc >= nused) continue;  // a set no slab started
+                float w[16];
+                tmem_ld16(tmem + lanes + (p0 + pi) * a.Np + b0, w);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += w[j];
+            }
+            if (row < r_count) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (b0 + j < a.batch)
+                        store_y(a.y, (b0 + j) * a.ldy + r_begin + row, v[j], a.y_f32 != 0);
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kSpTmemCols)
+                     : "memory");
+    }
+}
+
 using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -518,7 +861,7 @@ uint64_t spmm_tc_desc_hi(uint32_t lbo_enc)
 
 bool spmm_tc_applies(const SpmvProblem &p, int nsm)
 {
-    if (p.N != 2 || p.M != 4 || p.batch < 8 || p.batch > 32) return false;
+    if (p.N != 2 || p.M != 4 || p.batch < 1 || p.batch > 32) return false;
     if (p.K % kSlabPos != 0 || p.K / 2 > (1ll << 31) || p.rows < 1) return false;
     if (p.ldx % 8 != 0) return false;
     // tensor-map bases must be 16-byte aligned
@@ -529,8 +872,89 @@ bool spmm_tc_applies(const SpmvProblem &p, int nsm)
     return (p.rows + grid - 1) / grid <= kMaxRows;
 }
 
+// The sparse-operand variant (nm_spmm_sp_kernel); same maps and conditions.
+cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode, cudaStream_t s)
+{
+    EncodeTiled enc = encode_tiled_tc();
+    if (!enc) return cudaErrorNotSupported;
+    const int nsm = sm_count();
+    if (nsm <= 0) return cudaErrorInvalidDevice;
+    const int Np = p.batch <= 16 ? 16 : 32;
+    const int64_t Lv = p.K / 2;
+    const int64_t Lm = p.K / 32;
+    const int grid = static_cast<int>(std::min<int64_t>(p.rows, nsm));
+    const int box_rows = static_cast<int>(p.rows / grid + (p.rows % grid ? 1 : 0));
+    if (box_rows > kMaxRows) return cudaErrorNotSupported;
+    CUtensorMap tv, tm, tx;
+    if (!encode2d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.values, Lv, p.rows, Lv * 2, 64,
+                  box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode2d(enc, &tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, p.masks, Lm, p.rows, Lm * 4, 4,
+                  box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorNotSupported;
+    int x3d = 1;
+    if (!encode_x3d(enc, &tx, p.x, p.K, p.batch, p.ldx * 2, Np)) {
+        x3d = 0;
+        if (!encode2d(enc, &tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.batch, p.ldx * 2, 64,
+                      Np, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorNotSupported;
+    }
+    SpArgs a = {};
+    a.x3d = x3d;
+    a.y = p.y;
+    a.ldy = p.ldy;
+    a.rows = static_cast<int>(p.rows);
+    a.K = static_cast<int>(p.K);
+    a.batch = p.batch;
+    a.Np = Np;
+    a.row_base = static_cast<int>(p.rows / grid);
+    a.row_extra = static_cast<int>(p.rows % grid);
+    a.y_f32 = p.y_f32 ? 1 : 0;
+    a.idesc = spmm_tc_idesc(Np) | (1u << 2);  // sparse A
+    a.desc_hi = desc_hi;
+    a.meta_mode = meta_mode;
+    a.ntile = (box_rows + kTileM - 1) / kTileM;
+    // accumulator sets and metadata buffers: the tuning keys sp_acc and
+    // sp_mbufs, else as many as tensor memory holds
+    a.nacc = std::max(1, std::min(kSpMaxAccSets, bulk_tuning().sp_acc));
+    while (a.nacc > 1 && 4 * a.nacc * Np + a.ntile * 32 > static_cast<int>(kSpTmemCols)) --a.nacc;
+    a.meta_base = static_cast<uint32_t>(4 * a.nacc * Np);
+    const int fit = (static_cast<int>(kSpTmemCols) - static_cast<int>(a.meta_base)) / (a.ntile * 32);
+    a.nmbuf = std::min(kSpMaxMetaBufs, fit);
+    if (bulk_tuning().sp_mbufs > 0) a.nmbuf = std::min(a.nmbuf, bulk_tuning().sp_mbufs);
+    if (a.nmbuf < 1) return cudaErrorNotSupported;
+    // a stage: the loaded rows' values, their mask words, x.  The MMA reads
+    // all 128 rows of a tile; rows past the box read the bytes after it
+    // (their sums are never stored), and `slack` after the last stage keeps
+    // those reads inside the allocation.  Small stages make a deep ring: a
+    // stage is refilled only a full round trip (copy, metadata, MMA) after
+    // it was issued, so the bytes in flight per SM are the ring's.
+    a.x_bytes = 2 * Np * 128;
+    a.off_m = (box_rows * 128 + 1023) / 1024 * 1024;
+    a.off_x = a.off_m + (box_rows * 16 + 1023) / 1024 * 1024;
+    a.stage_bytes = a.off_x + a.x_bytes;
+    const int slack = std::max(0, a.ntile * kTileM * 128 - a.stage_bytes);
+    const int tail = 1024 + 512;
+    const int avail = max_dynamic_smem();
+    if (avail <= 0) return cudaErrorInvalidDevice;
+    a.S = std::min(kSpMaxStages, (avail - tail - slack) / a.stage_bytes);
+    if (a.S < 2) return cudaErrorNotSupported;
+    a.off_bar = a.S * a.stage_bytes + slack;
+    a.err = p.err;
+    const int smem = a.off_bar + tail;
+    static std::atomic<int> smem_set{0};
+    if (smem > smem_set.load(std::memory_order_relaxed)) {
+        cudaError_t e =
+            cudaFuncSetAttribute(nm_spmm_sp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        smem_set.store(smem, std::memory_order_relaxed);
+    }
+    nm_spmm_sp_kernel<<<grid, kSpThreads, smem, s>>>(tv, tm, tx, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s)
 {
+    if (bulk_tuning().tc_sp) return launch_spmm_sp(p, desc_hi, bulk_tuning().sp_meta, s);
     EncodeTiled enc = encode_tiled_tc();
     if (!enc) return cudaErrorNotSupported;
     const int nsm = sm_count();

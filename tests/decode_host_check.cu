@@ -143,6 +143,67 @@ Result check_expand()
     return r;
 }
 
+// The sparse tensor-core metadata: every combination of valid 2:4 groups in
+// a mask word (sampled), each nibble's code = the positions of its two set
+// bits, lower first (mode 0) or swapped (mode 1).
+Result check_sp_meta()
+{
+    Result r;
+    const std::vector<uint32_t> gm = group_masks(2, 4);
+    uint64_t state = 0x2545F4914F6CDD1Dull;
+    for (int t = 0; t < 200000; ++t) {
+        state ^= state << 13;
+        state ^= state >> 7;
+        state ^= state << 17;
+        uint32_t m = 0, want0 = 0, want1 = 0;
+        uint64_t s = state;
+        for (int g = 0; g < 8; ++g) {
+            const uint32_t n = gm[s % gm.size()];
+            s /= gm.size();
+            m |= n << (4 * g);
+            int i0 = -1, i1 = -1;
+            for (int p = 0; p < 4; ++p)
+                if ((n >> p) & 1u) (i0 < 0 ? i0 : i1) = p;
+            want0 |= static_cast<uint32_t>(i0 | (i1 << 2)) << (4 * g);
+            want1 |= static_cast<uint32_t>(i1 | (i0 << 2)) << (4 * g);
+        }
+        for (int mode = 0; mode < 2; ++mode) {
+            ++r.checks;
+            const uint32_t got = nm::sp_meta_word(m, mode), want = mode ? want1 : want0;
+            if (got != want) {
+                if (r.fails < 5)
+                    std::printf("sp meta mode %d mask %08x: got %08x, want %08x\n", mode, m, got,
+                                want);
+                ++r.fails;
+            }
+        }
+    }
+    // lane interleave of rows r, r + 8: the word a lane stores gives, read
+    // back as the tensor cores read it (low lane: own low half = row r groups
+    // 0-3, partner's low half = row r groups 4-7; high lane: partner's high
+    // half = row r+8 groups 0-3, own high half = groups 4-7), each row's own
+    // metadata word
+    for (int t = 0; t < 100000; ++t) {
+        state ^= state << 13;
+        state ^= state >> 7;
+        state ^= state << 17;
+        const uint32_t wr = static_cast<uint32_t>(state), wr8 = static_cast<uint32_t>(state >> 32);
+        const uint32_t lane_lo = nm::sp_meta_lane_word(wr, wr8, false);   // stored in lane r
+        const uint32_t lane_hi = nm::sp_meta_lane_word(wr8, wr, true);    // stored in lane r + 8
+        const uint32_t read_r = (lane_lo & 0xFFFFu) | ((lane_hi & 0xFFFFu) << 16);
+        const uint32_t read_r8 = (lane_lo >> 16) | (lane_hi & 0xFFFF0000u);
+        ++r.checks;
+        if (read_r != wr || read_r8 != wr8) {
+            if (r.fails < 5)
+                std::printf("sp lane words %08x %08x: read back %08x %08x\n", wr, wr8, read_r,
+                            read_r8);
+            ++r.fails;
+        }
+    }
+    std::printf("2:4s metadata %ld checks, %ld failures\n", r.checks, r.fails);
+    return r;
+}
+
 }  // namespace
 
 int main()
@@ -156,6 +217,7 @@ int main()
     fails += check_all<4, 4>(0).fails;
     fails += check_all<8, 8>(0).fails;
     fails += check_expand().fails;
+    fails += check_sp_meta().fails;
     std::printf(fails ? "FAIL\n" : "OK\n");
     return fails ? 1 : 0;
 }

@@ -35,6 +35,6 @@ def test_mask_decode_and_gather_on_the_host(tmp_path):
     run = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert run.returncode == 0 and run.stdout.strip().endswith("OK"), run.stdout + run.stderr
     # every pattern reported, none with failures
-    for pat in ("2:4", "1:4", "2:8", "4:8", "1:8", "4:4", "8:8", "2:4x"):
+    for pat in ("2:4", "1:4", "2:8", "4:8", "1:8", "4:4", "8:8", "2:4x", "2:4s"):
         line = [l for l in run.stdout.splitlines() if l.startswith(pat + " ")]
         assert line and line[0].endswith(" 0 failures"), run.stdout

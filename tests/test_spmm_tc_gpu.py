@@ -1,5 +1,6 @@
-"""GPU parity of the tensor-core 2:4 product (tcgen05, A operand expanded
-into tensor memory) against the CPU oracle.
+"""GPU parity of the tensor-core 2:4 products (tcgen05: A expanded into
+tensor memory, or the packed values as the sparse operand of
+tcgen05.mma.sp) against the CPU oracle.
 
 The path is taken by default for 2:4 products at batch 8 on layers with more
 than 128 rows per SM; the forced tuning ``tc=1`` (read once per process, so
@@ -73,12 +74,15 @@ CASES = [
     (-257, 256, 8, False, True),      # 257 rows a CTA: CUDA-core kernels
     (37000, 384, 8, True, False),
     (3000, 4000, 8, False, True),     # K not a multiple of 128
-    (5000, 2048, 5, False, True),     # batch below 8: CUDA-core kernels
+    (5000, 2048, 5, False, True),     # batch 5 (x padded to 16 rows)
 ]
 
 
-def test_tensor_core_path_forced():
-    env = dict(os.environ, NM_BULK_TUNE="tc=1")
+@pytest.mark.parametrize("tune", ["tc=1", "tc=1,tc_sp=1"], ids=["expanded", "sparse_operand"])
+def test_tensor_core_path_forced(tune):
+    """Every case through the tensor-core product, A either expanded into
+    tensor memory or taken as the sparse operand of tcgen05.mma.sp."""
+    env = dict(os.environ, NM_BULK_TUNE=tune)
     r = subprocess.run([sys.executable, "-c", _CHILD, ROOT, json.dumps(CASES)], env=env,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-2000:]
