@@ -506,14 +506,17 @@ def _eager_time(run, n, warmup=3):
 def _libnm_kernel(rows, batch):
     """Which kernel libnm runs for a 2:4 product with K a multiple of 128
     (the library's routing rule, restated for the report; NM_BULK_TUNE tc=0/1
-    overrides it there and here)."""
+    and tc_sp=0 override it there and here)."""
     tune = dict(kv.split("=", 1) for kv in os.environ.get("NM_BULK_TUNE", "").split(",")
                 if "=" in kv)
-    tc = int(tune.get("tc", "-1"))
+    tc, sp = int(tune.get("tc", "-1")), int(tune.get("tc_sp", "1"))
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
-    fits = batch == 8 and (rows + nsm - 1) // nsm <= 256
-    if tc != 0 and fits and (tc == 1 or rows > 128 * nsm):
-        return "tensor-core 2:4 product (tcgen05)"
+    per_sm = (rows + nsm - 1) // nsm
+    auto = ((batch >= 3 and per_sm > 128) or (batch >= 5 and per_sm > 80)
+            or (batch >= 8 and per_sm > 40))
+    if tc != 0 and per_sm <= 256 and (tc == 1 or auto):
+        return ("tensor-core 2:4 product (tcgen05.mma.sp, packed values as the sparse operand)"
+                if sp else "tensor-core 2:4 product (tcgen05, A expanded into tensor memory)")
     return "CUDA-core row kernel"
 
 

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 150 /* 1.5.0 */
+#define NM_VERSION 160 /* 1.6.0 */
 #define NM_MAX_BATCH 8
 #define NM_MAX_GROUP 8
 
@@ -185,14 +185,17 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
  *   x  fp16 [batch][ldx], device; ldx >= K; with batch > 1, ldx must be a
  *      multiple of 8 so that every vector starts 16-byte aligned.
  *   y  y_type [batch][ldy], device; ldy >= rows.  Row b of y receives A x_b.
- * Same semantics and errors as nm_spmv.  At batch 8, a 2:4 matrix with more
- * than 128 rows per SM (K a multiple of 128, at most 256 rows per SM, x and
- * the packed arrays 16-byte aligned) is multiplied on the tensor cores: its
- * groups are expanded to dense fp16 on chip and multiplied with fp32
- * accumulation in another order, within the same error bound and
- * deterministic from call to call; it does not use programmatic dependent
- * launch.  NM_BULK_TUNE=tc=0 turns this off, tc=1 takes it for every 2:4
- * product at batch 8 that it can run.
+ * Same semantics and errors as nm_spmv.  A 2:4 matrix with K a multiple of
+ * 128, at most 256 rows per SM and x and the packed arrays 16-byte aligned
+ * is multiplied on the tensor cores when that is faster: from batch 3 with
+ * more than 128 rows per SM, from batch 5 with more than 80, at batch 8 with
+ * more than 40.  The packed values are then the compressed operand of the
+ * sparse tensor-core MMA (the mask bits become its metadata on chip) and
+ * products are summed with fp32 accumulation in another order, within the
+ * same error bound and deterministic from call to call; that path does not
+ * use programmatic dependent launch.  NM_BULK_TUNE=tc=0 turns it off, tc=1
+ * takes it for every 2:4 product it can run; tc_sp=0 selects the earlier
+ * variant that expands the groups to dense fp16 in tensor memory.
  */
 nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
                           void *y, int64_t ldy, int batch, nm_dtype y_type,
@@ -215,7 +218,7 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
  * the matrix); matrices that differ in N, M or K are NM_ERR_INVALID_ARG.
  * When the shapes cannot share a launch, or every product takes the
  * tensor-core path of nm_spmv_batched, the products are launched one by one,
- * with the same results.  Asynchronous, allocates nothing, may be
+ * with the same results (then each on the kernel nm_spmv_batched picks).  Asynchronous, allocates nothing, may be
  * captured in a CUDA graph; the products' y must not overlap.
  */
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,

@@ -229,15 +229,22 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
 // One product on the best kernel that applies: the row kernel (any batch;
 // K a multiple of 128), the chunk-column kernel (when no row plan fits in
 // shared memory), the direct-load kernel, the scalar kernel.
-// 2:4 at batch 8 on layers with more than 128 rows an SM: the tensor-core
-// product (the CUDA-core kernel is instruction-bound there).  Tuning key tc
-// forces it on (1) or off (0).
+// 2:4 products with several vectors go to the tensor-core product where it
+// is faster (measured on the decode shapes): it streams near the HBM rate
+// when each SM has two 128-row MMA tiles (more than 128 rows per SM) from
+// batch 3, while with one tile each 128-position slab costs ~0.45 us, which
+// pays only from batch 5 with more than 80 rows per SM or at batch 8 with
+// more than 40; the CUDA-core row kernel, instruction-bound from batch 3,
+// takes the rest.  Tuning key tc forces it on (1) or off (0).
 bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
 {
     const int tc = nm::spmm_tc_mode(lbo_enc);
     const int nsm = nm::sm_count();
-    return tc != 0 && nm::spmm_tc_applies(p, nsm) &&
-           (tc == 1 || (p.batch == 8 && p.rows > 128LL * nsm));
+    if (tc == 0 || nsm <= 0 || !nm::spmm_tc_applies(p, nsm)) return false;
+    if (tc == 1) return true;
+    const int64_t per_sm = (p.rows + nsm - 1) / nsm;
+    return (p.batch >= 3 && per_sm > 128) || (p.batch >= 5 && per_sm > 80) ||
+           (p.batch >= 8 && per_sm > 40);
 }
 
 nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)

@@ -272,24 +272,28 @@ struct BulkTuning {
                                    // patterns whose chunk spans 32 positions; 0: never; -1: auto
     int rows_l2pre_bytes = 0;      // weight bytes per CTA warmed in L2 before that wait
     // tensor-core product (2:4, batch 8 and up; nm_spmm_tc.cu)
-    int tc = -1;                   // 1: wherever it applies, 0: never, -1: batch 8 with
-                                   // more than 128 rows a CTA (two MMA tiles)
+    int tc = -1;                   // 1: wherever it applies, 0: never, -1: by batch and
+                                   // rows per SM (takes_tensor_cores in nm_api.cu)
     int tc_lbo = 1;                // encoded leading-byte-offset field of its descriptors
     // Test of the device-side failure path only: the row kernel issues no
     // copies and waits 2 ms (not 2 s) on its slot barriers, so every wait
     // runs out, the error word is set and the kernel returns.
     int wait_fault_test = 0;
-    int tc_sp = 0;                 // 1: the tensor-core product takes the packed values as the
-                                   // sparse A operand (tcgen05.mma.sp) instead of expanding them
+    int tc_sp = 1;                 // 1: the tensor-core product takes the packed values as the
+                                   // sparse A operand (tcgen05.mma.sp); 0: it expands them into
+                                   // tensor memory (the earlier, slower kernel)
     int sp_meta = 0;               // metadata nibble order of that path (0: i0 | i1 << 2)
     int sp_acc = 2;                // accumulator sets each MMA issuer of that path rotates over
     int sp_mbufs = 0;              // its metadata buffers (0: as many as tensor memory holds)
+    int sp_spin = 1;               // 1: its metadata warps and MMA issuers spin; 0: suspend
+    int sp_sel = 0;                // 1: its four metadata words of a slab in consecutive columns,
+                                   // the MMA picking one with the descriptor's sparsity selector
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows_two, rows (row-per-warp kernel),
-// ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs
+// ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs, sp_sel, sp_spin
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 

@@ -511,6 +511,9 @@ struct SpArgs {
     int stage_bytes, x_bytes, off_bar;
     int x3d;
     int meta_mode;            // sp_meta_word mode
+    int spin;                 // 1: metadata warps and MMA issuers spin on their barriers
+    int meta_sel;             // 1: an MMA's metadata word is column kk of the buffer's
+                              // group, chosen by the descriptor's sparsity selector
     int nacc;                 // accumulator sets per issuer (independent chains of MMAs)
     int nmbuf;                // metadata buffers in tensor memory
     uint32_t meta_base;       // first metadata column (after 4 * nacc * Np accumulators)
@@ -518,6 +521,13 @@ struct SpArgs {
 };
 
 // D[tmem_d] (+)= A[a_desc] * B[b_desc], A 2:4-sparse with metadata at tmem_e.
+// The metadata warps' and MMA issuers' waits: spinning (tuning key sp_spin=1,
+// the default) or suspending until the phase completes.
+__device__ __forceinline__ bool sp_wait(uint64_t *bar, uint32_t parity, int spin)
+{
+    return spin ? mbar_spin(bar, parity) : mbar_wait(bar, parity);
+}
+
 __device__ __forceinline__ void mma_sp_ss(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t tmem_e, uint32_t idesc, uint32_t accumulate)
 {
@@ -533,6 +543,15 @@ __device__ __forceinline__ void mma_sp_ss(uint32_t tmem_d, uint64_t a_desc, uint
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r0)
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r0)
+                 : "memory");
+}
+
+// Four consecutive 32-bit columns into this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                         uint32_t r3)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
                  : "memory");
 }
 
@@ -667,8 +686,8 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
             const uint32_t stage0 = smem_addr(smem);
             for (int k = 0; k < nslab; ++k) {
                 if (*failed) break;
-                if (!mbar_spin(&fullv[s], ps) || !mbar_spin(&fullx[s], ps) ||
-                    !mbar_spin(&mfull[d], pd)) {
+                if (!sp_wait(&fullv[s], ps, a.spin) || !sp_wait(&fullx[s], ps, a.spin) ||
+                    !sp_wait(&mfull[d], pd, a.spin)) {
                     *failed = 1;
                     atomicOr(a.err, kDevErrPipeTimeout);
                     break;
@@ -682,12 +701,14 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                     // the slab; x: 32 positions, box kk / 2, 64-byte step kk % 2
                     const uint32_t aoff = static_cast<uint32_t>(kk) * 32u;
                     const uint32_t boff = (kk >> 1) * (a.x_bytes / 2) + (kk & 1) * 64;
-                    const uint32_t meta = tmem + sp_meta_col(a.meta_base, a.ntile, d, t, kk);
+                    const uint32_t meta =
+                        tmem + sp_meta_col(a.meta_base, a.ntile, d, t, a.meta_sel ? 0 : kk);
+                    const uint32_t idesc = a.meta_sel ? (a.idesc | static_cast<uint32_t>(kk)) : a.idesc;
                     // slab k adds into set k % nacc: the first slab of each set
                     // starts it
                     mma_sp_ss(dcol0 + static_cast<uint32_t>(ka * a.Np),
                               a.desc_hi | ((av + aoff) >> 4), a.desc_hi | ((xb + boff) >> 4),
-                              meta, a.idesc, (k >= a.nacc || kk > kk0) ? 1u : 0u);
+                              meta, idesc, (k >= a.nacc || kk > kk0) ? 1u : 0u);
                 }
                 commit_to(&done[qd]);
                 if (++s == S) {
@@ -714,8 +735,8 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         for (int k = 0; k < nslab; ++k) {
             int ok = 0;
             if (lane == 0)
-                ok = !*failed && mbar_spin(&fullm[s], ps) &&
-                     (k < NB || mbar_spin(&done[qn], pn));
+                ok = !*failed && sp_wait(&fullm[s], ps, a.spin) &&
+                     (k < NB || sp_wait(&done[qn], pn, a.spin));
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0 && !*failed) {
@@ -732,14 +753,25 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
             const uint4 m4 =
                 *reinterpret_cast<const uint4 *>(smem + s * a.stage_bytes + a.off_m + rs * 16);
             const uint32_t mw[4] = {m4.x, m4.y, m4.z, m4.w};
+            uint32_t lw[4];
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 // this row's metadata word for MMA kk, interleaved with that of
                 // the row 8 apart (sp_meta_lane_word)
                 const uint32_t own = sp_meta_word(mw[kk], a.meta_mode);
                 const uint32_t partner = __shfl_xor_sync(0xffffffffu, own, 8);
-                tmem_st1(tlanes + sp_meta_col(a.meta_base, a.ntile, d, t, kk),
-                         sp_meta_lane_word(own, partner, (lane & 8) != 0));
+                lw[kk] = sp_meta_lane_word(own, partner, (lane & 8) != 0);
+            }
+            // the four words at their 8-aligned columns (or, with the selector
+            // layout, in four consecutive columns); one 32-column store of the
+            // four measured no faster than four single-column ones
+            if (a.meta_sel) {
+                tmem_st4(tlanes + sp_meta_col(a.meta_base, a.ntile, d, t, 0), lw[0], lw[1], lw[2],
+                         lw[3]);
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tmem_st1(tlanes + sp_meta_col(a.meta_base, a.ntile, d, t, kk), lw[kk]);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -891,11 +923,15 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
         !encode2d(enc, &tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, p.masks, Lm, p.rows, Lm * 4, 4,
                   box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorNotSupported;
+    // x: only the batch's rows, rounded up to 8 (one 128-byte-swizzle atom);
+    // the MMA reads Np rows, and the rows past Bx read whatever follows: they
+    // only feed accumulator columns that are never stored
+    const int Bx = (p.batch + 7) / 8 * 8;
     int x3d = 1;
-    if (!encode_x3d(enc, &tx, p.x, p.K, p.batch, p.ldx * 2, Np)) {
+    if (!encode_x3d(enc, &tx, p.x, p.K, p.batch, p.ldx * 2, Bx)) {
         x3d = 0;
         if (!encode2d(enc, &tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.batch, p.ldx * 2, 64,
-                      Np, CU_TENSOR_MAP_SWIZZLE_128B))
+                      Bx, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorNotSupported;
     }
     SpArgs a = {};
@@ -912,6 +948,8 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     a.idesc = spmm_tc_idesc(Np) | (1u << 2);  // sparse A
     a.desc_hi = desc_hi;
     a.meta_mode = meta_mode;
+    a.meta_sel = bulk_tuning().sp_sel;
+    a.spin = bulk_tuning().sp_spin;
     a.ntile = (box_rows + kTileM - 1) / kTileM;
     // accumulator sets and metadata buffers: the tuning keys sp_acc and
     // sp_mbufs, else as many as tensor memory holds
@@ -928,11 +966,11 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     // those reads inside the allocation.  Small stages make a deep ring: a
     // stage is refilled only a full round trip (copy, metadata, MMA) after
     // it was issued, so the bytes in flight per SM are the ring's.
-    a.x_bytes = 2 * Np * 128;
+    a.x_bytes = 2 * Bx * 128;  // two 64-position planes of Bx rows
     a.off_m = (box_rows * 128 + 1023) / 1024 * 1024;
     a.off_x = a.off_m + (box_rows * 16 + 1023) / 1024 * 1024;
     a.stage_bytes = a.off_x + a.x_bytes;
-    const int slack = std::max(0, a.ntile * kTileM * 128 - a.stage_bytes);
+    const int slack = std::max({0, a.ntile * kTileM * 128 - a.stage_bytes, (Np - Bx) * 128});
     const int tail = 1024 + 512;
     const int avail = max_dynamic_smem();
     if (avail <= 0) return cudaErrorInvalidDevice;
