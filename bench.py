@@ -43,7 +43,9 @@ FALLBACK_HBM_GBS = 6400.0
 # DRAM bytes (read + write) per launch, averaged over the launches of one
 # step, from an ncu capture of that step taken with the current kernels;
 # workloads without an entry report null.
-TRAFFIC_PER_LAUNCH = {}
+TRAFFIC_PER_LAUNCH = {
+    ("llama31_8b_block", "2:4", 1, "fused"): 61.481e6,  # 12 launches of the fused step
+}
 
 
 def parse_args(argv=None):
