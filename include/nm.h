@@ -192,8 +192,8 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
  * more than 40.  The packed values are then the compressed operand of the
  * sparse tensor-core MMA (the mask bits become its metadata on chip) and
  * products are summed with fp32 accumulation in another order, within the
- * same error bound and deterministic from call to call; that path does not
- * use programmatic dependent launch.  NM_BULK_TUNE=tc=0 turns it off, tc=1
+ * same error bound and deterministic from call to call; that path overlaps
+ * the preceding kernel as nm_spmv does.  NM_BULK_TUNE=tc=0 turns it off, tc=1
  * takes it for every 2:4 product it can run; tc_sp=0 selects the earlier
  * variant that expands the groups to dense fp16 in tensor memory.
  */

@@ -584,6 +584,11 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc + 1);
     volatile int *failed = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
+    // Programmatic dependent launch: the next kernel in the stream may start
+    // its own prologue and weight copies now; this one reads x and writes y
+    // only after the previous kernel has completed (griddepcontrol.wait in
+    // the x producer and before the epilogue).
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const int r_begin = cta * a.row_base + min(cta, a.row_extra);
@@ -627,6 +632,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         // own byte count on its own barrier.
         const int role = warp - kSpProdWarp;
         uint64_t *full = role == 0 ? fullv : role == 1 ? fullm : fullx;
+        if (role == 2) pdl_wait();  // x may be the previous kernel's output
         if (lane == 0) {
             const CUtensorMap *map = role == 0 ? &tm_vals : role == 1 ? &tm_masks : &tm_x;
             prefetch_map(map);
@@ -792,6 +798,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     if (!ok && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
     const bool go = __syncthreads_and(ok && *failed == 0) != 0;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    pdl_wait();  // y may still be read by the previous kernel
     if (go && warp < nconv) {
         const int t = warp >> 2, q = warp & 3;
         const int row = t * kTileM + 32 * q + lane;
@@ -986,8 +993,17 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
         if (e != cudaSuccess) return e;
         smem_set.store(smem, std::memory_order_relaxed);
     }
-    nm_spmm_sp_kernel<<<grid, kSpThreads, smem, s>>>(tv, tm, tx, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kSpThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = bulk_tuning().pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, nm_spmm_sp_kernel, tv, tm, tx, a);
 }
 
 cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s)
