@@ -21,11 +21,13 @@ the SM clocks seen during the timed region.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -121,33 +123,46 @@ def host_cores():
 
 
 class ClockSampler:
-    """nvidia-smi samples (SM clock, reasons) while the GPU runs."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (SM clock, reasons) while the GPU runs.  nvidia-smi
+    writes them, timestamped, to a file that is read only when a summary is
+    asked for: no Python thread runs beside the timed loops (one that woke
+    every sample would take the GIL from the end-to-end loop's host thread)."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int, period_ms: int = 20):
         self.index, self.period_ms = index, period_ms
-        self.samples, self.proc, self.thread = [], None, None
+        self.proc, self.out = None, None
 
     def start(self):
         try:
+            self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
                  "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=self.out, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-            return self
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
+    @property
+    def samples(self):
+        """(epoch seconds, [index, sm, max sm, power, active, 4 reasons]) each."""
+        if self.out is None:
+            return []
+        self.out.seek(0)
+        rows = []
+        for line in self.out.read().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append((time.time(), parts))
+            if len(parts) < 10:
+                continue  # a line nvidia-smi is still writing
+            try:
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((t, parts[1:]))
+        return rows
 
     def wait_first(self, timeout: float = 3.0):
         """Block until nvidia-smi has printed a sample (its start-up is done,
@@ -164,13 +179,12 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-        if self.thread is not None:
-            self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float, window: str = "timed region"):
-        sel = [p for t, p in self.samples if t0 <= t <= t1]
+        samples = self.samples
+        sel = [p for t, p in samples if t0 <= t <= t1]
         if not sel:
-            sel = [p for _, p in self.samples]
+            sel = [p for _, p in samples]
             window = "whole run (timed region shorter than the sampling period)"
         if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
@@ -505,7 +519,7 @@ def _eager_time(run, n, warmup=3):
     return statistics.median(times)
 
 
-def _libnm_kernel(rows, batch):
+def _libnm_kernel(rows, batch, K):
     """Which kernel libnm runs for a 2:4 product with K a multiple of 128
     (the library's routing rule, restated for the report; NM_BULK_TUNE tc=0/1
     and tc_sp=0 override it there and here)."""
@@ -514,8 +528,9 @@ def _libnm_kernel(rows, batch):
     tc, sp = int(tune.get("tc", "-1")), int(tune.get("tc_sp", "1"))
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     per_sm = (rows + nsm - 1) // nsm
-    auto = ((batch >= 3 and per_sm > 128) or (batch >= 5 and per_sm > 80)
-            or (batch >= 8 and per_sm > 40))
+    w = rows * K
+    auto = ((batch >= 5 and w >= 4 << 20) or (batch == 4 and w > 24_000_000)
+            or (batch == 3 and w >= 32 << 20 and (K >= 12288 or per_sm > 128)))
     if tc != 0 and per_sm <= 256 and (tc == 1 or auto):
         return ("tensor-core 2:4 product (tcgen05.mma.sp, packed values as the sparse operand)"
                 if sp else "tensor-core 2:4 product (tcgen05, A expanded into tensor memory)")
@@ -550,7 +565,7 @@ def crossover_pass(batches=(1, 2, 4, 8, 16, 32, 64)):
         row = {"batch": B}
         if B <= nm.NM_MAX_BATCH:
             try:
-                row["libnm_kernel"] = _libnm_kernel(rows, B)
+                row["libnm_kernel"] = _libnm_kernel(rows, B, K)
             except Exception as e:  # a label only: never costs the timing
                 row["libnm_kernel"] = "unknown (%s)" % type(e).__name__
             y = torch.empty(B, rows, dtype=torch.float16, device="cuda")
@@ -1234,7 +1249,7 @@ def layer_one(args, rows, K, N, M, B):
            "us": med * 1e6, "us_p10": p10 * 1e6, "us_p90": p90 * 1e6,
            "algorithmic_bytes": nbytes, "gbs": nbytes / med / 1e9,
            "frac_of_peak": nbytes / med / 1e9 / peak, "peak_gbs": peak, "peak_kind": peak_kind,
-           "kernel": _libnm_kernel(rows, B) if (N, M) == (2, 4) and K % 128 == 0 else None}
+           "kernel": _libnm_kernel(rows, B, K) if (N, M) == (2, 4) and K % 128 == 0 else None}
     print(json.dumps(out), flush=True)
     del mats, A, x, y
     torch.cuda.empty_cache()

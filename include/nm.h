@@ -187,9 +187,11 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
  *   y  y_type [batch][ldy], device; ldy >= rows.  Row b of y receives A x_b.
  * Same semantics and errors as nm_spmv.  A 2:4 matrix with K a multiple of
  * 128, at most 256 rows per SM and x and the packed arrays 16-byte aligned
- * is multiplied on the tensor cores when that is faster: from batch 3 with
- * more than 128 rows per SM, from batch 5 with more than 80, at batch 8 with
- * more than 40.  The packed values are then the compressed operand of the
+ * is multiplied on the tensor cores when that is faster: from batch 5 on
+ * layers of at least 4 Mi weights (rows x K), at batch 4 above 24 M, at
+ * batch 3 from 32 Mi with K >= 12288 or more than 128 rows per SM.  Layers of
+ * at most one 128-row tile per SM then split K over a thread-block cluster
+ * of 2-8 CTAs (batch <= 8).  The packed values are then the compressed operand of the
  * sparse tensor-core MMA (the mask bits become its metadata on chip) and
  * products are summed with fp32 accumulation in another order, within the
  * same error bound and deterministic from call to call; that path overlaps

@@ -286,14 +286,18 @@ struct BulkTuning {
     int sp_acc = 2;                // accumulator sets each MMA issuer of that path rotates over
     int sp_mbufs = 0;              // its metadata buffers (0: as many as tensor memory holds)
     int sp_spin = 1;               // 1: its metadata warps and MMA issuers spin; 0: suspend
+    int sp_split = 1;              // 1: one-tile layers split K over clusters of 2-8 CTAs
     int sp_sel = 0;                // 1: its four metadata words of a slab in consecutive columns,
                                    // the MMA picking one with the descriptor's sparsity selector
+    int sp_stages = 0;             // its ring's stages at most (0: as many as shared memory holds)
+    int sp_tmem = 512;             // tensor-memory columns a CTA of it allocates (256 or 512)
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows_two, rows (row-per-warp kernel),
-// ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs, sp_sel, sp_spin
+// ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs, sp_sel, sp_spin, sp_split,
+// sp_stages, sp_tmem
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 

@@ -52,6 +52,9 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "sp_mbufs") && v >= 1 && v <= 12) t.sp_mbufs = v;
         else if (!std::strcmp(tok, "sp_sel") && (v == 0 || v == 1)) t.sp_sel = v;
         else if (!std::strcmp(tok, "sp_spin") && (v == 0 || v == 1)) t.sp_spin = v;
+        else if (!std::strcmp(tok, "sp_split") && (v == 0 || v == 1)) t.sp_split = v;
+        else if (!std::strcmp(tok, "sp_stages") && v >= 0 && v <= 32 && v != 1) t.sp_stages = v;
+        else if (!std::strcmp(tok, "sp_tmem") && (v == 256 || v == 512)) t.sp_tmem = v;
         else if (!std::strcmp(tok, "rows_l2pre") && v >= 0) t.rows_l2pre_bytes = v;
         else if (!std::strcmp(tok, "tc") && (v == -1 || v == 0 || v == 1)) t.tc = v;
         else if (!std::strcmp(tok, "tc_lbo") && v >= 0 && v < 16384) t.tc_lbo = v;

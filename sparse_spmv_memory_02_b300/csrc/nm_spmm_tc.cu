@@ -486,7 +486,7 @@ constexpr int kSpThreads = 32 * (kSpConvWarps + kSpProdWarps + kSpMmaWarps);
 constexpr int kSpMaxStages = 32;      // ring stages (a stage holds only the rows it loads)
 constexpr int kSpMaxMetaBufs = 12;    // metadata buffers (ntile x 4 MMAs each)
 constexpr int kSpMaxAccSets = 4;      // accumulator sets an issuer rotates over, slab by slab
-constexpr uint32_t kSpTmemCols = 512; // accumulators first, then metadata
+constexpr uint32_t kSpTmemCols = 512; // most columns a CTA allocates: accumulators, then metadata
 // Tensor memory: issuer i's accumulator set j at column (i * nacc + j) * Np
 // (4 issuers); from meta_base, each MMA's metadata word in its own column,
 // 8-column aligned: meta_base + 8 * ((d * ntile + t) * 4 + kk) for buffer d,
@@ -511,6 +511,10 @@ struct SpArgs {
     int stage_bytes, x_bytes, off_bar;
     int x3d;
     int meta_mode;            // sp_meta_word mode
+    int ksplit;               // CTAs (one cluster) sharing a 128-row tile, each a part of K
+                              // (1: no split, rows split evenly over the CTAs)
+    int off_part;             // K split: rank 0's region for ranks 1..'s sums, [r - 1][row][8]
+    uint32_t tmem_cols;       // tensor-memory columns allocated (256 or 512)
     int spin;                 // 1: metadata warps and MMA issuers spin on their barriers
     int meta_sel;             // 1: an MMA's metadata word is column kk of the buffer's
                               // group, chosen by the descriptor's sparsity selector
@@ -521,6 +525,44 @@ struct SpArgs {
 };
 
 // D[tmem_d] (+)= A[a_desc] * B[b_desc], A 2:4-sparse with metadata at tmem_e.
+// The cluster barrier in two halves: every thread of every CTA of the cluster
+// arrives (release) and later waits (acquire); what a CTA wrote to shared
+// memory before its arrive is visible to the others after their wait.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// The shared::cluster address of this CTA's shared address `a` in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+// Four floats into another CTA's shared memory (16-byte aligned shared::cluster
+// address); the 16 bytes complete on that CTA's mbarrier `bar` (its
+// shared::cluster address).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a0, float a1, float a2, float a3,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+        ::"r"(addr), "f"(a0), "f"(a1), "f"(a2), "f"(a3), "r"(bar)
+        : "memory");
+}
+
+// Eight fp32 columns of this warp's 32 tensor-memory lanes, without waiting
+// (tmem_wait_ld before the registers are read).
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // The metadata warps' and MMA issuers' waits: spinning (tuning key sp_spin=1,
 // the default) or suspending until the phase completes.
 __device__ __forceinline__ bool sp_wait(uint64_t *bar, uint32_t parity, int spin)
@@ -568,7 +610,12 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         a.S < 2 || a.S > kSpMaxStages ||
         a.nmbuf < 1 || a.nmbuf > kSpMaxMetaBufs || a.nacc < 1 || a.nacc > kSpMaxAccSets ||
         a.meta_base < static_cast<uint32_t>(4 * a.nacc * a.Np) ||
-        sp_meta_col(a.meta_base, a.ntile, a.nmbuf - 1, a.ntile - 1, 3) >= kSpTmemCols) {
+        (a.tmem_cols != 256 && a.tmem_cols != kSpTmemCols) ||
+        sp_meta_col(a.meta_base, a.ntile, a.nmbuf - 1, a.ntile - 1, 3) >= a.tmem_cols ||
+        (a.ksplit > 1 &&
+         (a.ksplit > 8 || gridDim.x % a.ksplit != 0 || a.row_base != kTileM || a.row_extra != 0 ||
+          a.Np != 16 || a.K / kSlabPos < a.ksplit || (a.off_part & 15) ||
+          a.off_part + (a.ksplit - 1) * kTileM * 32 > a.off_bar))) {
         if (threadIdx.x == 0) atomicOr(a.err, kDevErrSmemAlign);
         return;
     }
@@ -581,7 +628,8 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     uint64_t *done = fullx + kSpMaxStages;       // [Q] MMA -> producers, metadata warps
     uint64_t *mfull = done + kSpMaxStages + 1;   // [nmbuf] metadata warps -> MMA
     uint64_t *acc = mfull + kSpMaxMetaBufs;      // MMA -> epilogue
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc + 1);
+    uint64_t *part = acc + 1;                    // K split, rank 0: ranks 1..'s sums landed
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(part + 1);
     volatile int *failed = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     // Programmatic dependent launch: the next kernel in the stream may start
@@ -591,40 +639,69 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
-    const int r_begin = cta * a.row_base + min(cta, a.row_extra);
-    const int r_count = a.row_base + (cta < a.row_extra ? 1 : 0);
+    // K split: the a.ksplit consecutive CTAs of a cluster share one 128-row
+    // tile, CTA `rank` taking slabs [slab_lo, slab_lo + nslab)
+    const int rank = a.ksplit > 1 ? cta % a.ksplit : 0;
+    const int tile_id = cta / a.ksplit;
+    const int r_begin = a.ksplit > 1 ? tile_id * kTileM : cta * a.row_base + min(cta, a.row_extra);
+    const int r_count = a.ksplit > 1 ? min(kTileM, a.rows - r_begin)
+                                     : a.row_base + (cta < a.row_extra ? 1 : 0);
     const int ntile = (r_count + kTileM - 1) / kTileM;  // this CTA's tiles (<= a.ntile)
     const int nconv = 4 * ntile;                        // metadata warps at work
-    const int nslab = a.K / kSlabPos;
+    const int nslab_all = a.K / kSlabPos;
+    const int slab_lo = static_cast<int>(static_cast<int64_t>(rank) * nslab_all / a.ksplit);
+    const int nslab =
+        static_cast<int>(static_cast<int64_t>(rank + 1) * nslab_all / a.ksplit) - slab_lo;
     const int S = a.S;
     const int NB = a.nmbuf;
     const int Q = max(S, NB) + 1;  // exceeds both ring depths
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&fullv[s], 1);
-            mbar_init(&fullm[s], 1);
-            mbar_init(&fullx[s], 1);
+    // the tensor maps' descriptors start on their way now
+    if (warp == kSpProdWarp && lane < 3) prefetch_map(lane == 0 ? &tm_vals : lane == 1 ? &tm_masks : &tm_x);
+    // one thread a barrier (Q exceeds S and NB)
+    if (static_cast<int>(threadIdx.x) < Q) {
+        const int i = threadIdx.x;
+        if (i < S) {
+            mbar_init(&fullv[i], 1);
+            mbar_init(&fullm[i], 1);
+            mbar_init(&fullx[i], 1);
         }
-        for (int j = 0; j < Q; ++j) mbar_init(&done[j], kSpMmaWarps);  // one commit an issuer
-        for (int d = 0; d < NB; ++d) mbar_init(&mfull[d], nconv);
-        mbar_init(acc, kSpMmaWarps);
-        *failed = 0;
+        mbar_init(&done[i], kSpMmaWarps);  // one commit an issuer
+        if (i < NB) mbar_init(&mfull[i], nconv);
+        if (i == 0) {
+            mbar_init(acc, kSpMmaWarps);
+            mbar_init(part, 1);
+            *failed = 0;
+        }
         mbar_fence_init();
+        // rank 0 of a split expects ranks 1..'s sums: 32 bytes a row each
+        if (i == 0 && a.ksplit > 1 && rank == 0)
+            mbar_arrive_expect_tx(part, static_cast<uint32_t>((a.ksplit - 1) * kTileM * 32));
     }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr(tmem_slot)),
-                     "r"(kSpTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    // the cluster's barriers are initialised before any CTA of it writes to
+    // another (the matching wait is in the epilogue)
+    if (a.ksplit > 1) cluster_arrive();
     __syncthreads();
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = *tmem_slot;
 
-    if (warp >= kSpProdWarp && warp < kSpProdWarp + kSpProdWarps) {
+    // Tensor memory: warp 0 allocates it while the producers start their
+    // copies; the other warps that use it meet on barrier 2.
+    const bool producer = warp >= kSpProdWarp && warp < kSpProdWarp + kSpProdWarps;
+    uint32_t tmem = 0;
+    if (!producer) {
+        if (warp == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_addr(tmem_slot)),
+                         "r"(a.tmem_cols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        named_barrier_sync(2, kSpThreads - 32 * kSpProdWarps);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tmem = *tmem_slot;
+    }
+
+    if (producer) {
         // ------------------------------------------------ TMA producers
         // Three warps, one copy each a slab (values, mask words, x): issuing a
         // tensor copy blocks the issuing thread for a while, and the three
@@ -634,9 +711,8 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         uint64_t *full = role == 0 ? fullv : role == 1 ? fullm : fullx;
         if (role == 2) pdl_wait();  // x may be the previous kernel's output
         if (lane == 0) {
-            const CUtensorMap *map = role == 0 ? &tm_vals : role == 1 ? &tm_masks : &tm_x;
-            prefetch_map(map);
-            const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x);
+            const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x) %
+                              max(nslab, 1);
             const uint32_t box_rows = static_cast<uint32_t>(a.row_base + (a.row_extra ? 1 : 0));
             const uint32_t tx = role == 0 ? box_rows * 128u
                               : role == 1 ? box_rows * 16u
@@ -658,6 +734,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 uint8_t *st = smem + s * a.stage_bytes;
                 int ks = k + slab0;
                 if (ks >= nslab) ks -= nslab;
+                ks += slab_lo;
                 mbar_arrive_expect_tx(&full[s], tx);
                 if (role == 0) {
                     tma2d(st, &tm_vals, ks * 64, r_begin, &full[s]);
@@ -799,7 +876,67 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     const bool go = __syncthreads_and(ok && *failed == 0) != 0;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     pdl_wait();  // y may still be read by the previous kernel
-    if (go && warp < nconv) {
+    if (a.ksplit > 1) {
+        // K split (one tile, batch <= 8, so Np = 16 and 8 columns matter):
+        // ranks 1.. send their sums to rank 0's region with st.async, which
+        // counts them on rank 0's `part` barrier; rank 0 adds them in rank
+        // order.  Every rank sends (zeros after a failure) so that rank 0's
+        // wait always ends; the cluster wait makes rank 0's barrier
+        // initialisation visible first.
+        cluster_wait();
+        if (warp < 4) {
+            const int row = 32 * warp + lane;
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = 0.f;
+            if (go) {
+                // the sets slabs started (issuer i, set j at (i * nacc + j) * 16):
+                // up to 4 a batch, one wait each
+                const int nused = min(a.nacc, nslab);
+                const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+                for (int i = 0; i < kSpMmaWarps; ++i)
+                    for (int j0 = 0; j0 < nused; j0 += 4) {
+                        uint32_t r[4][8];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (j0 + jj < nused)
+                                tmem_ld8_nowait(lanes + (i * a.nacc + j0 + jj) * a.Np, r[jj]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            if (j0 + jj < nused)
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) v[c] += __uint_as_float(r[jj][c]);
+                    }
+            }
+            const uint32_t my_part = smem_addr(smem + a.off_part);
+            if (rank > 0) {
+                const uint32_t dst =
+                    cluster_map(my_part + static_cast<uint32_t>(((rank - 1) * kTileM + row) * 32), 0);
+                const uint32_t bar = cluster_map(smem_addr(part), 0);
+                st_async_v4(dst, v[0], v[1], v[2], v[3], bar);
+                st_async_v4(dst + 16, v[4], v[5], v[6], v[7], bar);
+            } else {
+                // ranks 1.. reach this point within their own bounded waits
+                bool landed = true;
+                if (lane == 0) landed = mbar_wait(part, 0, 8 * kWaitLimitNs);
+                landed = __shfl_sync(0xffffffffu, landed ? 1 : 0, 0) != 0;
+                if (!landed && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
+                const float *pp = reinterpret_cast<const float *>(smem + a.off_part);
+                for (int r = 1; r < a.ksplit; ++r) {
+                    const float4 p0 = *reinterpret_cast<const float4 *>(pp + ((r - 1) * kTileM + row) * 8);
+                    const float4 p1 = *reinterpret_cast<const float4 *>(pp + ((r - 1) * kTileM + row) * 8 + 4);
+                    v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+                    v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+                }
+                if (go && landed && row < r_count) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (j < a.batch) store_y(a.y, j * a.ldy + r_begin + row, v[j], a.y_f32 != 0);
+                }
+            }
+        }
+    } else if (go && warp < nconv) {
         const int t = warp >> 2, q = warp & 3;
         const int row = t * kTileM + 32 * q + lane;
         // the tile's partial sums: every accumulator set of issuers 2t, 2t + 1
@@ -831,7 +968,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kSpTmemCols)
+                     "r"(a.tmem_cols)
                      : "memory");
     }
 }
@@ -911,8 +1048,23 @@ bool spmm_tc_applies(const SpmvProblem &p, int nsm)
     return (p.rows + grid - 1) / grid <= kMaxRows;
 }
 
+cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta_mode,
+                                bool allow_split, cudaStream_t s);
+
+cudaError_t launch_spmm_sp_nosplit(const SpmvProblem &p, uint64_t desc_hi, int meta_mode,
+                                   cudaStream_t s)
+{
+    return launch_spmm_sp_impl(p, desc_hi, meta_mode, false, s);
+}
+
 // The sparse-operand variant (nm_spmm_sp_kernel); same maps and conditions.
 cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode, cudaStream_t s)
+{
+    return launch_spmm_sp_impl(p, desc_hi, meta_mode, true, s);
+}
+
+cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta_mode,
+                                bool allow_split, cudaStream_t s)
 {
     EncodeTiled enc = encode_tiled_tc();
     if (!enc) return cudaErrorNotSupported;
@@ -921,9 +1073,25 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     const int Np = p.batch <= 16 ? 16 : 32;
     const int64_t Lv = p.K / 2;
     const int64_t Lm = p.K / 32;
-    const int grid = static_cast<int>(std::min<int64_t>(p.rows, nsm));
-    const int box_rows = static_cast<int>(p.rows / grid + (p.rows % grid ? 1 : 0));
+    int grid = static_cast<int>(std::min<int64_t>(p.rows, nsm));
+    int box_rows = static_cast<int>(p.rows / grid + (p.rows % grid ? 1 : 0));
     if (box_rows > kMaxRows) return cudaErrorNotSupported;
+    // K split: when the rows give each SM at most one 128-row tile, a tile
+    // costs its MMA pipeline per slab whatever rows it holds, so full tiles
+    // are shared by clusters of 2-8 CTAs, each a part of K (up to 8 vectors).
+    int ksplit = 1;
+    const int64_t ntiles = (p.rows + kTileM - 1) / kTileM;
+    if (allow_split && bulk_tuning().sp_split && p.batch <= 8 && box_rows <= kTileM &&
+        ntiles * 2 <= nsm) {
+        ksplit = static_cast<int>(std::min<int64_t>(8, nsm / ntiles));
+        ksplit = std::min(ksplit, static_cast<int>(p.K / kSlabPos));  // at least one slab each
+        if (ksplit > 1) {
+            grid = static_cast<int>(ntiles) * ksplit;
+            box_rows = kTileM;
+        } else {
+            ksplit = 1;
+        }
+    }
     CUtensorMap tv, tm, tx;
     if (!encode2d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.values, Lv, p.rows, Lv * 2, 64,
                   box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -949,21 +1117,25 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     a.K = static_cast<int>(p.K);
     a.batch = p.batch;
     a.Np = Np;
-    a.row_base = static_cast<int>(p.rows / grid);
-    a.row_extra = static_cast<int>(p.rows % grid);
+    // the boxes' row count (what each copy delivers); with the K split every
+    // CTA loads a full tile and takes its rows from the tile index
+    a.row_base = ksplit > 1 ? kTileM : static_cast<int>(p.rows / grid);
+    a.row_extra = ksplit > 1 ? 0 : static_cast<int>(p.rows % grid);
     a.y_f32 = p.y_f32 ? 1 : 0;
     a.idesc = spmm_tc_idesc(Np) | (1u << 2);  // sparse A
     a.desc_hi = desc_hi;
     a.meta_mode = meta_mode;
     a.meta_sel = bulk_tuning().sp_sel;
+    a.ksplit = ksplit;
     a.spin = bulk_tuning().sp_spin;
     a.ntile = (box_rows + kTileM - 1) / kTileM;
     // accumulator sets and metadata buffers: the tuning keys sp_acc and
     // sp_mbufs, else as many as tensor memory holds
+    a.tmem_cols = static_cast<uint32_t>(bulk_tuning().sp_tmem);
     a.nacc = std::max(1, std::min(kSpMaxAccSets, bulk_tuning().sp_acc));
-    while (a.nacc > 1 && 4 * a.nacc * Np + a.ntile * 32 > static_cast<int>(kSpTmemCols)) --a.nacc;
+    while (a.nacc > 1 && 4 * a.nacc * Np + a.ntile * 32 > static_cast<int>(a.tmem_cols)) --a.nacc;
     a.meta_base = static_cast<uint32_t>(4 * a.nacc * Np);
-    const int fit = (static_cast<int>(kSpTmemCols) - static_cast<int>(a.meta_base)) / (a.ntile * 32);
+    const int fit = (static_cast<int>(a.tmem_cols) - static_cast<int>(a.meta_base)) / (a.ntile * 32);
     a.nmbuf = std::min(kSpMaxMetaBufs, fit);
     if (bulk_tuning().sp_mbufs > 0) a.nmbuf = std::min(a.nmbuf, bulk_tuning().sp_mbufs);
     if (a.nmbuf < 1) return cudaErrorNotSupported;
@@ -981,9 +1153,14 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     const int tail = 1024 + 512;
     const int avail = max_dynamic_smem();
     if (avail <= 0) return cudaErrorInvalidDevice;
-    a.S = std::min(kSpMaxStages, (avail - tail - slack) / a.stage_bytes);
+    // K split: rank 0 receives ranks 1..'s sums (4 KB each) in a region of
+    // its own, which the ring never uses
+    const int part_bytes = ksplit > 1 ? (ksplit - 1) * kTileM * 32 : 0;
+    a.S = std::min(kSpMaxStages, (avail - tail - slack - part_bytes) / a.stage_bytes);
+    if (bulk_tuning().sp_stages > 0) a.S = std::min(a.S, bulk_tuning().sp_stages);
     if (a.S < 2) return cudaErrorNotSupported;
-    a.off_bar = a.S * a.stage_bytes + slack;
+    a.off_part = a.S * a.stage_bytes + slack;  // 16-byte aligned (stages 1 KB, slack 128 B units)
+    a.off_bar = a.off_part + part_bytes;
     a.err = p.err;
     const int smem = a.off_bar + tail;
     static std::atomic<int> smem_set{0};
@@ -998,11 +1175,43 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     cfg.blockDim = dim3(kSpThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (bulk_tuning().pdl) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    if (ksplit > 1) {
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(ksplit);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+        // a cluster of that size must fit on the device at this shared-memory
+        // size (cached per size and device), else no split
+        static std::atomic<int> fits[64][9];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        int f = fits[dev][ksplit].load(std::memory_order_relaxed);
+        if (f == 0) {
+            cfg.attrs = attr;
+            cfg.numAttrs = nattr;
+            int nclusters = 0;
+            const cudaError_t e =
+                cudaOccupancyMaxActiveClusters(&nclusters, nm_spmm_sp_kernel, &cfg);
+            f = (e == cudaSuccess && nclusters > 0) ? 1 : -1;
+            if (e != cudaSuccess) cudaGetLastError();  // clear the sticky-free error state
+            fits[dev][ksplit].store(f, std::memory_order_relaxed);
+        }
+        if (f < 0) {
+            // relaunch without the split (rows evenly over the CTAs)
+            SpmvProblem q = p;
+            return launch_spmm_sp_nosplit(q, desc_hi, meta_mode, s);
+        }
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = bulk_tuning().pdl ? 1 : 0;
+    cfg.numAttrs = nattr;
     return cudaLaunchKernelEx(&cfg, nm_spmm_sp_kernel, tv, tm, tx, a);
 }
 

@@ -2,14 +2,17 @@
 tensor memory, or the packed values as the sparse operand of
 tcgen05.mma.sp) against the CPU oracle.
 
-The path is taken by default for 2:4 products at batch 8 on layers with more
-than 128 rows per SM; the forced tuning ``tc=1`` (read once per process, so
+The path is taken by default for 2:4 products from batch 3-5 on large enough
+layers (the routing rule in nm_api.cu); the forced tuning ``tc=1`` (read once per process, so
 run in a child) makes every 2:4 product with K a multiple of 128 and at most
 256 rows per CTA take it.  Shapes cover one row, fewer rows than SMs, ragged
 row splits, one and two 128-row MMA tiles (the second partial), the largest
 split that still fits (256 rows per CTA), splits just past it and K not a
 multiple of 128 (both fall back to the CUDA-core kernels), fp16 and fp32 y,
-and x and y with row strides wider than the matrix.
+x and y with row strides wider than the matrix, and for the sparse-operand
+product the K split: layers of at most one 128-row tile a SM give each tile
+to a cluster of 2-8 CTAs, each a share of K's slabs (even and uneven shares,
+a partial last tile, batch 1-8).
 """
 import json
 import os
@@ -75,13 +78,20 @@ CASES = [
     (37000, 384, 8, True, False),
     (3000, 4000, 8, False, True),     # K not a multiple of 128
     (5000, 2048, 5, False, True),     # batch 5 (x padded to 16 rows)
+    # the sparse-operand product's K split (clusters of CTAs sharing a tile)
+    (1000, 896, 4, False, True),      # clusters of 7, 7 slabs: one slab each
+    (1000, 640, 3, True, False),      # clusters of 5; last tile 104 rows
+    (4100, 1152, 8, False, True),     # clusters of 4 over 9 slabs (3, 2, 2, 2)
+    (8192, 1024, 1, False, True),     # batch 1, clusters of 2
 ]
 
 
-@pytest.mark.parametrize("tune", ["tc=1", "tc=1,tc_sp=1"], ids=["expanded", "sparse_operand"])
+@pytest.mark.parametrize("tune", ["tc=1,tc_sp=0", "tc=1,tc_sp=1", "tc=1,tc_sp=1,sp_split=0"],
+                         ids=["expanded", "sparse_operand", "sparse_operand_unsplit"])
 def test_tensor_core_path_forced(tune):
     """Every case through the tensor-core product, A either expanded into
-    tensor memory or taken as the sparse operand of tcgen05.mma.sp."""
+    tensor memory or taken as the sparse operand of tcgen05.mma.sp (with
+    and without the K split across a cluster)."""
     env = dict(os.environ, NM_BULK_TUNE=tune)
     r = subprocess.run([sys.executable, "-c", _CHILD, ROOT, json.dumps(CASES)], env=env,
                        capture_output=True, text=True, timeout=900)
