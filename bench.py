@@ -60,6 +60,9 @@ def parse_args(argv=None):
     p.add_argument("--pattern", default=None, help="N:M, default: the workload's first")
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--copies", type=int, default=3, help="rotating packed copies (L2 defeat)")
+    p.add_argument("--graph-steps", type=int, default=32,
+                   help="consecutive steps (decoder blocks) captured in one CUDA graph: 32 is "
+                        "one forward of a 32-block model such as Llama-3.1-8B")
     p.add_argument("--profile-steps", type=int, default=50, help="calls per layer in the per-layer pass")
     p.add_argument("--launch", choices=["fused", "unfused", "fused_silu"], default="fused",
                    help="fused: layers reading the same input (q/k/v, gate/up) share one "
@@ -334,6 +337,53 @@ def time_steps(streams, copies, steps, warmup, world, samples=20):
     t_wall1 = time.time()
     barrier(world)
     per_step = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 / max(1, bounds[i + 1] - bounds[i])
+                for i in range(samples)]
+    return ev[0].elapsed_time(ev[samples]) * 1e-3, per_step, t_wall0, t_wall1
+
+
+def capture_multi_step(streams, copies, nsteps):
+    """One CUDA graph of steps 0 .. nsteps - 1, step s on packed copy s % copies."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for s in range(nsteps):
+                streams[s % copies].run_eager()
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
+def time_graph_steps(streams, copies, per_graph, steps, warmup, world, samples=20):
+    """As time_steps, with `per_graph` consecutive steps in each CUDA graph
+    (a decode forward's blocks; the last replay takes the remainder), so the
+    timed region runs exactly `steps` steps.  The timed pieces are whole
+    replays."""
+    per_graph = max(1, min(per_graph, steps))
+    g = capture_multi_step(streams, copies, per_graph)
+    rem = steps % per_graph
+    reps = [(g, per_graph)] * (steps // per_graph)
+    if rem:
+        reps.append((capture_multi_step(streams, copies, rem), rem))
+    for _ in range(-(-max(1, warmup) // per_graph)):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    samples = max(1, min(samples, len(reps)))
+    bounds = [round(i * len(reps) / samples) for i in range(samples + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(samples + 1)]
+    t_wall0 = time.time()
+    ev[0].record()
+    for i in range(samples):
+        for r in range(bounds[i], bounds[i + 1]):
+            reps[r][0].replay()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    per_step = [ev[i].elapsed_time(ev[i + 1]) * 1e-3
+                / max(1, sum(n for _, n in reps[bounds[i]:bounds[i + 1]]))
                 for i in range(samples)]
     return ev[0].elapsed_time(ev[samples]) * 1e-3, per_step, t_wall0, t_wall1
 
@@ -630,15 +680,19 @@ def dense_pass(layers, copies, steps, warmup):
     return dt, dense_bytes, n
 
 
-def e2e_pass(layers, copies, steps, warmup, fused, silu=False):
-    """Through the public API with host buffers.  Every step: all of the
-    step's distinct input vectors are copied from one pinned host buffer into
-    one device buffer, the step's libnm launches run, all of its outputs are
-    copied into one pinned host buffer -- the two copies captured together
-    with the launches in one CUDA graph per weight copy -- and the host waits
-    for the outputs (a decode loop needs them before the next token).
-    Returns (mean seconds per step, per-step seconds, h2d bytes, d2h bytes)."""
+def e2e_pass(layers, copies, steps, warmup, fused, silu=False, per_graph=1):
+    """Through the public API with host buffers, `per_graph` steps (decoder
+    blocks) a forward, each block with its own input and output buffers.
+    Every forward: all of its blocks' input vectors are copied from one
+    pinned host buffer into one device buffer, the blocks' libnm launches
+    run, all of their outputs are copied into one pinned host buffer -- the
+    two copies captured together with the launches in one CUDA graph -- and
+    the host waits for the outputs (a decode loop needs them before the next
+    token).  Block i reads packed copy i % copies.  Returns (mean seconds per
+    step, per-step seconds of every forward, h2d bytes per step, d2h bytes
+    per step)."""
     from sparse_spmv_memory_02_b300.stream import LayerStream
+    G = max(1, min(per_graph, steps))
     srcs = []
     for L in layers:
         if not any(L["x"] is t for t in srcs):
@@ -653,46 +707,54 @@ def e2e_pass(layers, copies, steps, warmup, fused, silu=False):
     xoff, xn = layout(srcs)
     youts = [L["y"] for L in layers]
     yoff, yn = layout(youts)
-    x_dev = torch.zeros(xn, dtype=torch.float16, device="cuda")
-    y_dev = torch.zeros(yn, dtype=youts[0].dtype, device="cuda")
-    x_views = [x_dev[o:o + t.numel()].view(t.shape) for o, t in zip(xoff, srcs)]
-    y_views = [y_dev[o:o + t.numel()].view(t.shape) for o, t in zip(yoff, youts)]
-    for v, t in zip(x_views, srcs):
-        v.copy_(t)
+    x_dev = torch.zeros(G * xn, dtype=torch.float16, device="cuda")
+    y_dev = torch.zeros(G * yn, dtype=youts[0].dtype, device="cuda")
+    blocks = []
+    for i in range(G):
+        xv = [x_dev[i * xn + o:i * xn + o + t.numel()].view(t.shape) for o, t in zip(xoff, srcs)]
+        yv = [y_dev[i * yn + o:i * yn + o + t.numel()].view(t.shape) for o, t in zip(yoff, youts)]
+        for v, t in zip(xv, srcs):
+            v.copy_(t)
+        xs = [xv[next(k for k, t in enumerate(srcs) if t is L["x"])] for L in layers]
+        blocks.append(LayerStream([L["mats"][i % copies] for L in layers], xs, yv,
+                                  fuse_shared_input=fused,
+                                  silu_pairs=silu_pairs(layers) if silu else ()))
     x_host = x_dev.cpu().pin_memory()
-    y_host = torch.empty(yn, dtype=y_dev.dtype).pin_memory()
-    xs = [x_views[next(i for i, t in enumerate(srcs) if t is L["x"])] for L in layers]
-    graphs = []
-    for c in range(copies):
-        st = LayerStream([L["mats"][c] for L in layers], xs, y_views, fuse_shared_input=fused,
-                         silu_pairs=silu_pairs(layers) if silu else ())
-        st.run_eager()
-        torch.cuda.synchronize()
+    y_host = torch.empty(G * yn, dtype=y_dev.dtype).pin_memory()
+    for b in blocks[:2]:
+        b.run_eager()
+    torch.cuda.synchronize()
+
+    def forward_graph(n):
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
             with torch.cuda.graph(g, stream=side):
-                x_dev.copy_(x_host, non_blocking=True)
-                st.run_eager()
-                y_host.copy_(y_dev, non_blocking=True)
+                x_dev[:n * xn].copy_(x_host[:n * xn], non_blocking=True)
+                for b in blocks[:n]:
+                    b.run_eager()
+                y_host[:n * yn].copy_(y_dev[:n * yn], non_blocking=True)
         torch.cuda.current_stream().wait_stream(side)
-        graphs.append(g)
+        return g
+    reps = [(forward_graph(G), G)] * (steps // G)
+    if steps % G:
+        reps.append((forward_graph(steps % G), steps % G))
     cur = torch.cuda.current_stream()
-    for s in range(max(3, warmup)):
-        graphs[s % copies].replay()
+    for s in range(max(3, -(-warmup // G))):
+        reps[0][0].replay()
         cur.synchronize()
     per = []
     t0 = time.perf_counter()
-    for s in range(steps):
+    for g, n in reps:
         ts = time.perf_counter()
-        graphs[s % copies].replay()
+        g.replay()
         cur.synchronize()
-        per.append(time.perf_counter() - ts)
+        per.append((time.perf_counter() - ts) / n)
     dt = (time.perf_counter() - t0) / steps
     h2d = sum(t.numel() * t.element_size() for t in srcs)
     d2h = sum(t.numel() * t.element_size() for t in youts)
-    del graphs
+    del reps
     return dt, per, h2d, d2h
 
 
@@ -900,14 +962,17 @@ def config_block(args, wl, N, M, copies, layers_desc):
     return {"workload": wl.key, "title": wl.title, "pattern": "%d:%d" % (N, M),
             "batch": args.batch, "layers": layers_desc,
             "l2": "rotating %d packed copies of the step's weights (> 3x the 126 MB L2)" % copies,
-            "launch": "one CUDA graph per step: %s" % {
+            "launch": "%s: %s" % ("one CUDA graph per %d steps (a %d-block forward)"
+                                  % (args.graph_steps, args.graph_steps)
+                                  if getattr(args, "graph_steps", 1) > 1
+                                  else "one CUDA graph per step", {
                 "fused": "q/k/v and gate/up each one nm_spmv_group launch (they read the same "
                          "input), o and down one nm_spmv launch each",
                 "fused_silu": "q/k/v one nm_spmv_group launch, o and down one nm_spmv launch "
                               "each, gate/up one nm_spmv_gate_up_silu launch writing "
                               "silu(gate x) * (up x)",
                 "unfused": "one nm_spmv launch per layer"}.get(getattr(args, "launch", ""),
-                                                               "one nm_spmv launch per layer"),
+                                                               "one nm_spmv launch per layer")),
             "weights": "synthetic N(0,0.02), top-N |w| per group of M along K",
             "activations": ("synthetic N(0,1), 1% outlier channels x20; q/k/v share one input "
                             "vector, gate/up another" if wl.outliers else "synthetic N(0,1)")}
@@ -974,15 +1039,21 @@ def run_ours(args, world, rank, local):
     step_b = variant_bytes[args.launch]
     others = [k for k in variants if k != args.launch]
 
+    G = max(1, args.graph_steps)
     sampler = ClockSampler(local).start().wait_first() if rank == 0 else None
-    dt, step_samples, t_wall0, t_wall1 = time_steps(streams, copies, args.steps, args.warmup,
-                                                    world)
+    dt, step_samples, t_wall0, t_wall1 = time_graph_steps(streams, copies, G, args.steps,
+                                                          args.warmup, world)
     dt = max_over_ranks(dt, world)
     launches = streams[0].launches * args.steps
+    # the same steps with one CUDA graph a step (a graph boundary every block)
+    sdt, _, _, _ = time_steps(streams, copies, args.steps, args.warmup, world)
+    sdt = max_over_ranks(sdt, world)
+    one_graph_per_step = {"us_per_step": sdt / args.steps * 1e6,
+                          "value": world * step_b * args.steps / sdt / 1e9}
     # the other launch structures of the same step, same protocol
     other_launch = {}
     for k in others:
-        odt, _, _, _ = time_steps(variants[k], copies, args.steps, args.warmup, world)
+        odt, _, _, _ = time_graph_steps(variants[k], copies, G, args.steps, args.warmup, world)
         odt = max_over_ranks(odt, world)
         other_launch[k] = {"launches_per_step": variants[k][0].launches,
                            "us_per_step": odt / args.steps * 1e6,
@@ -991,17 +1062,28 @@ def run_ours(args, world, rank, local):
     # end to end right after the device-timed steps, before the other legs
     e2e = None
     if not args.no_e2e:
-        et, eper, h2d, d2h = e2e_pass(layers, copies, max(20, min(args.steps, 500)), args.warmup,
+        e_steps = max(20, min(args.steps, 640))
+        et, eper, h2d, d2h = e2e_pass(layers, copies, e_steps, args.warmup,
                                       fused=args.launch != "unfused",
-                                      silu=args.launch == "fused_silu")
+                                      silu=args.launch == "fused_silu", per_graph=G)
         ep10, emed, ep90 = percentiles(eper)
         e2e = {"value": step_b / et / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "us_per_step": et * 1e6,
                "us_per_step_p10": ep10 * 1e6, "us_per_step_p50": emed * 1e6,
                "us_per_step_p90": ep90 * 1e6,
-               "path": "one CUDA graph per step: pinned host x -> one device buffer, the "
-                       "step's libnm launches (%s), all y -> one pinned host buffer; the host "
-                       "waits for y every step (wall clock)" % args.launch}
+               "path": "one CUDA graph per forward of %d steps (blocks), each block its own "
+                       "input and output buffers: every block's x from one pinned host buffer "
+                       "-> device, the blocks' libnm launches (%s), every block's y -> one "
+                       "pinned host buffer; the host waits for the outputs once per forward "
+                       "(wall clock)" % (G, args.launch)}
+        bt, bper, _, _ = e2e_pass(layers, copies, max(20, min(args.steps, 500)), args.warmup,
+                                  fused=args.launch != "unfused",
+                                  silu=args.launch == "fused_silu", per_graph=1)
+        bp10, bmed, bp90 = percentiles(bper)
+        e2e["host_wait_every_step"] = {
+            "value": step_b / bt / 1e9, "us_per_step": bt * 1e6, "us_per_step_p10": bp10 * 1e6,
+            "us_per_step_p50": bmed * 1e6, "us_per_step_p90": bp90 * 1e6,
+            "path": "one CUDA graph per step with its copies; the host waits every step"}
 
     # each layer alone, L2-cold, for the per-layer figures
     l2_bytes = l2
@@ -1140,6 +1222,7 @@ def run_ours(args, world, rank, local):
         "configs": configs,
         "frac_of_peak": value / world / peak,
         "peak_gbs": peak, "peak_kind": peak_kind,
+        "one_graph_per_step": one_graph_per_step,
         "launch": dict({"structure": args.launch, "launches_per_step": streams[0].launches,
                         "groups": [[layers[i]["name"] for i in g] for g in streams[0].groups]},
                        **other_launch),
@@ -1149,8 +1232,9 @@ def run_ours(args, world, rank, local):
                      "kernel": "nm_spmv_rows_kernel (every one of the %d launches of a step)"
                                % streams[0].launches,
                      "note": "achieved = algorithmic bytes per launch / average launch time over "
-                             "the timed steps (CUDA events on the replay stream; the step's "
-                             "launches are all this kernel, so this equals the step's GB/s); "
+                             "the timed steps (CUDA events on the replay stream, %d steps a "
+                             "CUDA graph; the step's launches are all this kernel, so this "
+                             "equals the step's GB/s); " % G +
                              "peak = %s copy bandwidth (read+write); a read-only stream can "
                              "exceed it" % peak_kind},
         "dense_gemv": dense,

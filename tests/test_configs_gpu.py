@@ -75,6 +75,28 @@ def test_config2_llama31_8b_block(fused):
         _check_layer(wl, L, 2, 4, 1)
 
 
+def test_config2_llama31_8b_block_forward_graph():
+    """The headline's timed structure: several blocks (steps) in one CUDA
+    graph rotating over packed copies.  After a replay every copy's last
+    step has run; the outputs (written by the last step) must match the
+    oracle, and the same replay again gives the same bits."""
+    wl = nm_synth.WORKLOADS["llama31_8b_block"]
+    layers = bench.build_workload(wl, 2, 4, 1, copies=2)
+    streams = bench.capture_step_graphs(layers, 2, fused=True)
+    g = bench.capture_multi_step(streams, 2, 5)
+    for L in layers:
+        L["y"].fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert nm.nm_device_errors() == 0
+    first = [L["y"].clone() for L in layers]
+    for L in layers:
+        _check_layer(wl, L, 2, 4, 1, check_pack=False)
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, L["y"]) for a, L in zip(first, layers))
+
+
 @pytest.mark.parametrize("N,M", [(2, 4), (4, 8), (1, 4), (2, 8)])
 def test_config3_qwen3_14b_mlp_pattern_sweep(N, M):
     wl = nm_synth.WORKLOADS["qwen3_14b_mlp"]
