@@ -579,8 +579,8 @@ def _libnm_kernel(rows, batch, K):
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     per_sm = (rows + nsm - 1) // nsm
     w = rows * K
-    auto = ((batch >= 5 and w >= 4 << 20) or (batch == 4 and w > 24_000_000)
-            or (batch == 3 and w >= 32 << 20 and (K >= 12288 or per_sm > 128)))
+    auto = ((batch >= 5 and w >= 4 << 20) or (batch in (3, 4) and w > 24_000_000)
+            or (batch == 2 and w >= 128 << 20 and per_sm <= 128))
     if tc != 0 and per_sm <= 256 and (tc == 1 or auto):
         return ("tensor-core 2:4 product (tcgen05.mma.sp, packed values as the sparse operand)"
                 if sp else "tensor-core 2:4 product (tcgen05, A expanded into tensor memory)")

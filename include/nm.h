@@ -188,10 +188,10 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
  * Same semantics and errors as nm_spmv.  A 2:4 matrix with K a multiple of
  * 128, at most 256 rows per SM and x and the packed arrays 16-byte aligned
  * is multiplied on the tensor cores when that is faster: from batch 5 on
- * layers of at least 4 Mi weights (rows x K), at batch 4 above 24 M, at
- * batch 3 from 32 Mi with K >= 12288 or more than 128 rows per SM.  Layers of
- * at most one 128-row tile per SM then split K over a thread-block cluster
- * of 2-8 CTAs (batch <= 8).  The packed values are then the compressed operand of the
+ * layers of at least 4 Mi weights (rows x K), at batch 3-4 above 24 M, at
+ * batch 2 from 128 Mi with at most 128 rows per SM.  Layers of at most one
+ * 128-row tile per SM then split K over thread-block clusters of 2, 4 or 8
+ * CTAs (batch <= 8).  The packed values are then the compressed operand of the
  * sparse tensor-core MMA (the mask bits become its metadata on chip) and
  * products are summed with fp32 accumulation in another order, within the
  * same error bound and deterministic from call to call; that path overlaps

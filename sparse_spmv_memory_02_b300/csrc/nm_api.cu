@@ -231,16 +231,15 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
 // shared memory), the direct-load kernel, the scalar kernel.
 // 2:4 products with several vectors go to the tensor-core product where it
 // is faster (measured on the decode shapes, each layer alone).  Its time
-// hardly depends on the batch (up to 8): a fixed ~4 us a launch plus the
-// weights at 4.5-5.9 TB/s (a layer of at most one 128-row tile a SM splits
-// K over a cluster, so every SM streams full tiles).  The CUDA-core row
-// kernel is instruction-bound from batch 3 and slows with every vector.
-// Measured crossovers: from batch 5 the tensor cores win on every layer of
-// at least 4 M weights; at batch 4 on layers above 24 M weights (4096 x
-// 4096 still goes to the row kernel, 5120 x 5120 is a tie); at batch 3 only
-// on long rows (K >= 12288: 4096 x 14336, 8192 x 28672, 5120 x 25600) and on
-// tall layers of two tiles a SM (28672 x 8192), while 8192 x 8192 is still
-// 3 % faster on the row kernel.  Tuning key tc forces it on (1) or off (0).
+// hardly depends on the batch (up to 8): ~4.5 us a launch plus the weights
+// at up to ~6.1 TB/s (layers of at most one 128-row tile a SM split K over
+// clusters of 2-8 CTAs).  The CUDA-core row kernel is instruction-bound from
+// batch 3 and slows with every vector.  Measured crossovers: from batch 5
+// the tensor cores win on every layer of at least 4 Mi weights; at batch 3
+// and 4 on layers above 24 M (5120 x 5120 and larger; 4096 x 4096 and
+// 1024 x 8192 stay on the row kernel); at batch 2 only on the largest split
+// layers (8192 x 28672: 43 against 58 us; 8192 x 8192 is a tie, 28672 x
+// 8192 slightly slower).  Tuning key tc forces it on (1) or off (0).
 bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
 {
     const int tc = nm::spmm_tc_mode(lbo_enc);
@@ -250,8 +249,8 @@ bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
     const int64_t weights = p.rows * p.K;
     const int64_t per_sm = (p.rows + nsm - 1) / nsm;
     if (p.batch >= 5) return weights >= (4ll << 20);
-    if (p.batch == 4) return weights > 24ll * 1000 * 1000;
-    if (p.batch == 3) return weights >= (32ll << 20) && (p.K >= 12288 || per_sm > 128);
+    if (p.batch >= 3) return weights > 24ll * 1000 * 1000;
+    if (p.batch == 2) return weights >= (128ll << 20) && per_sm <= 128;
     return false;
 }
 

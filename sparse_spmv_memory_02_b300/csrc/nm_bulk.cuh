@@ -291,13 +291,15 @@ struct BulkTuning {
                                    // the MMA picking one with the descriptor's sparsity selector
     int sp_stages = 0;             // its ring's stages at most (0: as many as shared memory holds)
     int sp_tmem = 512;             // tensor-memory columns a CTA of it allocates (256 or 512)
+    int sp_k = 0;                  // its K split's cluster size (0: chosen by shape)
+    int sp_units = 0;              // its K split's row units at least (0: one a tile or tile pair)
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows_two, rows (row-per-warp kernel),
 // ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs, sp_sel, sp_spin, sp_split,
-// sp_stages, sp_tmem
+// sp_stages, sp_tmem, sp_k, sp_units
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 

@@ -55,6 +55,8 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "sp_split") && (v == 0 || v == 1)) t.sp_split = v;
         else if (!std::strcmp(tok, "sp_stages") && v >= 0 && v <= 32 && v != 1) t.sp_stages = v;
         else if (!std::strcmp(tok, "sp_tmem") && (v == 256 || v == 512)) t.sp_tmem = v;
+        else if (!std::strcmp(tok, "sp_k") && v >= 0 && v <= 8 && v != 1) t.sp_k = v;
+        else if (!std::strcmp(tok, "sp_units") && v >= 0) t.sp_units = v;
         else if (!std::strcmp(tok, "rows_l2pre") && v >= 0) t.rows_l2pre_bytes = v;
         else if (!std::strcmp(tok, "tc") && (v == -1 || v == 0 || v == 1)) t.tc = v;
         else if (!std::strcmp(tok, "tc_lbo") && v >= 0 && v < 16384) t.tc_lbo = v;

@@ -511,7 +511,7 @@ struct SpArgs {
     int stage_bytes, x_bytes, off_bar;
     int x3d;
     int meta_mode;            // sp_meta_word mode
-    int ksplit;               // CTAs (one cluster) sharing a 128-row tile, each a part of K
+    int ksplit;               // CTAs (one cluster) sharing a unit of rows, each a part of K
                               // (1: no split, rows split evenly over the CTAs)
     int off_part;             // K split: rank 0's region for ranks 1..'s sums, [r - 1][row][8]
     uint32_t tmem_cols;       // tensor-memory columns allocated (256 or 512)
@@ -613,9 +613,10 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         (a.tmem_cols != 256 && a.tmem_cols != kSpTmemCols) ||
         sp_meta_col(a.meta_base, a.ntile, a.nmbuf - 1, a.ntile - 1, 3) >= a.tmem_cols ||
         (a.ksplit > 1 &&
-         (a.ksplit > 8 || gridDim.x % a.ksplit != 0 || a.row_base != kTileM || a.row_extra != 0 ||
-          a.Np != 16 || a.K / kSlabPos < a.ksplit || (a.off_part & 15) ||
-          a.off_part + (a.ksplit - 1) * kTileM * 32 > a.off_bar))) {
+         (a.ksplit > 8 || gridDim.x % a.ksplit != 0 ||
+          a.row_base + (a.row_extra ? 1 : 0) > kTileM * a.ntile || a.Np != 16 ||
+          a.K / kSlabPos < a.ksplit || (a.off_part & 15) ||
+          a.off_part + (a.ksplit - 1) * kTileM * a.ntile * 32 > a.off_bar))) {
         if (threadIdx.x == 0) atomicOr(a.err, kDevErrSmemAlign);
         return;
     }
@@ -639,13 +640,14 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
-    // K split: the a.ksplit consecutive CTAs of a cluster share one 128-row
-    // tile, CTA `rank` taking slabs [slab_lo, slab_lo + nslab)
+    // K split: the a.ksplit consecutive CTAs of a cluster share one unit of
+    // rows (one or two 128-row tiles), CTA `rank` taking slabs [slab_lo,
+    // slab_lo + nslab).  Rows are spread evenly over the units (CTAs without
+    // the split).
     const int rank = a.ksplit > 1 ? cta % a.ksplit : 0;
-    const int tile_id = cta / a.ksplit;
-    const int r_begin = a.ksplit > 1 ? tile_id * kTileM : cta * a.row_base + min(cta, a.row_extra);
-    const int r_count = a.ksplit > 1 ? min(kTileM, a.rows - r_begin)
-                                     : a.row_base + (cta < a.row_extra ? 1 : 0);
+    const int unit = cta / a.ksplit;
+    const int r_begin = unit * a.row_base + min(unit, a.row_extra);
+    const int r_count = a.row_base + (unit < a.row_extra ? 1 : 0);
     const int ntile = (r_count + kTileM - 1) / kTileM;  // this CTA's tiles (<= a.ntile)
     const int nconv = 4 * ntile;                        // metadata warps at work
     const int nslab_all = a.K / kSlabPos;
@@ -674,9 +676,10 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
             *failed = 0;
         }
         mbar_fence_init();
-        // rank 0 of a split expects ranks 1..'s sums: 32 bytes a row each
+        // rank 0 of a split expects ranks 1..'s sums: 32 bytes for each row
+        // of its tiles (the ranks of a cluster share the unit, so its tiles)
         if (i == 0 && a.ksplit > 1 && rank == 0)
-            mbar_arrive_expect_tx(part, static_cast<uint32_t>((a.ksplit - 1) * kTileM * 32));
+            mbar_arrive_expect_tx(part, static_cast<uint32_t>((a.ksplit - 1) * nconv * 32 * 32));
     }
     // the cluster's barriers are initialised before any CTA of it writes to
     // another (the matching wait is in the epilogue)
@@ -877,24 +880,28 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     pdl_wait();  // y may still be read by the previous kernel
     if (a.ksplit > 1) {
-        // K split (one tile, batch <= 8, so Np = 16 and 8 columns matter):
-        // ranks 1.. send their sums to rank 0's region with st.async, which
-        // counts them on rank 0's `part` barrier; rank 0 adds them in rank
-        // order.  Every rank sends (zeros after a failure) so that rank 0's
-        // wait always ends; the cluster wait makes rank 0's barrier
-        // initialisation visible first.
+        // K split (batch <= 8, so Np = 16 and 8 columns matter): ranks 1..
+        // send their sums to rank 0's region with st.async, which counts them
+        // on rank 0's `part` barrier; rank 0 adds them in rank order.  Every
+        // rank sends (zeros after a failure) so that rank 0's wait always
+        // ends; the cluster wait makes rank 0's barrier initialisation
+        // visible first.
         cluster_wait();
-        if (warp < 4) {
-            const int row = 32 * warp + lane;
+        if (warp < nconv) {
+            const int t = warp >> 2, q = warp & 3;
+            const int row = t * kTileM + 32 * q + lane;  // row in the unit
             float v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = 0.f;
             if (go) {
-                // the sets slabs started (issuer i, set j at (i * nacc + j) * 16):
-                // up to 4 a batch, one wait each
+                // the tile's sets that slabs started (issuer i, set j at
+                // (i * nacc + j) * 16; issuers 2t, 2t + 1 with two tiles, else
+                // all four): up to 4 a batch, one wait each
+                const int i0 = ntile == 2 ? 2 * t : 0;
+                const int ni = ntile == 2 ? 2 : kSpMmaWarps;
                 const int nused = min(a.nacc, nslab);
-                const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-                for (int i = 0; i < kSpMmaWarps; ++i)
+                const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * q) << 16);
+                for (int i = i0; i < i0 + ni; ++i)
                     for (int j0 = 0; j0 < nused; j0 += 4) {
                         uint32_t r[4][8];
 #pragma unroll
@@ -909,10 +916,13 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                                 for (int c = 0; c < 8; ++c) v[c] += __uint_as_float(r[jj][c]);
                     }
             }
+            // rank r's sums at [r - 1][row] in rows of 32 bytes, kTileM * a.ntile
+            // rows a rank
+            const int rank_rows = kTileM * a.ntile;
             const uint32_t my_part = smem_addr(smem + a.off_part);
             if (rank > 0) {
-                const uint32_t dst =
-                    cluster_map(my_part + static_cast<uint32_t>(((rank - 1) * kTileM + row) * 32), 0);
+                const uint32_t dst = cluster_map(
+                    my_part + static_cast<uint32_t>(((rank - 1) * rank_rows + row) * 32), 0);
                 const uint32_t bar = cluster_map(smem_addr(part), 0);
                 st_async_v4(dst, v[0], v[1], v[2], v[3], bar);
                 st_async_v4(dst + 16, v[4], v[5], v[6], v[7], bar);
@@ -924,8 +934,9 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 if (!landed && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
                 const float *pp = reinterpret_cast<const float *>(smem + a.off_part);
                 for (int r = 1; r < a.ksplit; ++r) {
-                    const float4 p0 = *reinterpret_cast<const float4 *>(pp + ((r - 1) * kTileM + row) * 8);
-                    const float4 p1 = *reinterpret_cast<const float4 *>(pp + ((r - 1) * kTileM + row) * 8 + 4);
+                    const float *src = pp + ((r - 1) * rank_rows + row) * 8;
+                    const float4 p0 = *reinterpret_cast<const float4 *>(src);
+                    const float4 p1 = *reinterpret_cast<const float4 *>(src + 4);
                     v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
                     v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
                 }
@@ -1048,23 +1059,111 @@ bool spmm_tc_applies(const SpmvProblem &p, int nsm)
     return (p.rows + grid - 1) / grid <= kMaxRows;
 }
 
-cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta_mode,
-                                bool allow_split, cudaStream_t s);
-
-cudaError_t launch_spmm_sp_nosplit(const SpmvProblem &p, uint64_t desc_hi, int meta_mode,
-                                   cudaStream_t s)
+// The sparse kernel may take `bytes` of dynamic shared memory (set once per
+// device, at the device's opt-in maximum, which every launch stays under).
+bool sp_allow_smem(int bytes)
 {
-    return launch_spmm_sp_impl(p, desc_hi, meta_mode, false, s);
+    static std::atomic<int> done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (done[dev].load(std::memory_order_relaxed) >= bytes) return true;
+    if (cudaFuncSetAttribute(nm_spmm_sp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
+        return false;
+    done[dev].store(bytes, std::memory_order_relaxed);
+    return true;
+}
+
+// Clusters of k CTAs of the sparse kernel (one CTA an SM) that can be
+// resident at once (cached per device and k; 0 if none or unknown).
+int sp_resident_clusters(int k)
+{
+    static std::atomic<int> cache[64][9];
+    int dev = 0;
+    if (k < 2 || k > 8 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int c = cache[dev][k].load(std::memory_order_relaxed);
+    if (c != 0) return c > 0 ? c : 0;
+    const int avail = max_dynamic_smem();
+    const int nsm = sm_count();
+    int n = 0;
+    if (avail > 0 && nsm >= k && sp_allow_smem(avail)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(nsm / k * k));
+        cfg.blockDim = dim3(kSpThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(avail);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(k);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, nm_spmm_sp_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();  // not a sticky error: clear it
+            n = 0;
+        }
+    }
+    cache[dev][k].store(n > 0 ? n : -1, std::memory_order_relaxed);
+    return n;
+}
+
+struct SpSplit {
+    int k;           // CTAs a cluster (1: no split)
+    int64_t units;   // row units (CTAs without the split, clusters with it)
+    int box_rows;    // rows of the largest unit
+};
+
+// How the sparse kernel lays a product over the SMs.  Without the split the
+// rows are spread over min(rows, nsm) CTAs; with it, units of one or two
+// 128-row tiles are each shared by a cluster of k = 2, 4 or 8 CTAs, each
+// streaming 1/k of K's slabs.  Measured on B300: a CTA's slab costs ~0.43 us
+// with one tile and ~0.61 us with two whatever rows they hold (the MMA
+// pipeline's round trip, below the HBM rate for small tiles), and a CTA
+// streams at most ~55 GB/s, all of them ~6.2 TB/s; the plan with the least
+// estimated time is taken, the smaller cluster on a tie.  Clusters of 3, 5,
+// 6 or 7 are not used: the GPU held only ~40 clusters of 3 at once where the
+// occupancy query promised 48, so part of the grid ran in a second wave.
+SpSplit sp_plan(const SpmvProblem &p, int nsm)
+{
+    const int64_t nslab = p.K / kSlabPos;
+    const double bytes = static_cast<double>(p.rows) * static_cast<double>(p.K) * 1.125;
+    auto estimate = [&](int k, int64_t units, int box_rows) {
+        const int nt = (box_rows + kTileM - 1) / kTileM;
+        const double t_slab = static_cast<double>((nslab + k - 1) / k) * (nt == 1 ? 0.43 : 0.61);
+        const double ctas = static_cast<double>(units * k);
+        const double t_bw = std::max(bytes / 6.2e6, bytes / (ctas * 55e3));
+        return std::max(t_slab, t_bw);
+    };
+    SpSplit best;
+    best.k = 1;
+    best.units = std::min<int64_t>(p.rows, nsm);
+    best.box_rows = static_cast<int>((p.rows + best.units - 1) / best.units);
+    double t_best = estimate(1, best.units, best.box_rows);
+    const BulkTuning &tu = bulk_tuning();
+    if (!tu.sp_split || p.batch > 8) return best;
+    for (int k = 2; k <= 8; k *= 2) {
+        if (tu.sp_k > 0 && k != tu.sp_k) continue;
+        if (k > nslab) break;
+        for (int nt = 1; nt <= 2; ++nt) {
+            int64_t units = (p.rows + kTileM * nt - 1) / (kTileM * nt);
+            if (tu.sp_units > 0) units = std::max<int64_t>(units, std::min<int64_t>(tu.sp_units, p.rows));
+            if (units * k > nsm || units > sp_resident_clusters(k)) continue;
+            const int box_rows = static_cast<int>((p.rows + units - 1) / units);
+            if (box_rows > kTileM * nt) continue;
+            const double t = estimate(k, units, box_rows);
+            if (t < 0.97 * t_best || (tu.sp_k > 0 && best.k == 1)) {
+                best.k = k;
+                best.units = units;
+                best.box_rows = box_rows;
+                t_best = t;
+            }
+        }
+    }
+    return best;
 }
 
 // The sparse-operand variant (nm_spmm_sp_kernel); same maps and conditions.
 cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode, cudaStream_t s)
-{
-    return launch_spmm_sp_impl(p, desc_hi, meta_mode, true, s);
-}
-
-cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta_mode,
-                                bool allow_split, cudaStream_t s)
 {
     EncodeTiled enc = encode_tiled_tc();
     if (!enc) return cudaErrorNotSupported;
@@ -1073,25 +1172,12 @@ cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta
     const int Np = p.batch <= 16 ? 16 : 32;
     const int64_t Lv = p.K / 2;
     const int64_t Lm = p.K / 32;
-    int grid = static_cast<int>(std::min<int64_t>(p.rows, nsm));
-    int box_rows = static_cast<int>(p.rows / grid + (p.rows % grid ? 1 : 0));
-    if (box_rows > kMaxRows) return cudaErrorNotSupported;
-    // K split: when the rows give each SM at most one 128-row tile, a tile
-    // costs its MMA pipeline per slab whatever rows it holds, so full tiles
-    // are shared by clusters of 2-8 CTAs, each a part of K (up to 8 vectors).
-    int ksplit = 1;
-    const int64_t ntiles = (p.rows + kTileM - 1) / kTileM;
-    if (allow_split && bulk_tuning().sp_split && p.batch <= 8 && box_rows <= kTileM &&
-        ntiles * 2 <= nsm) {
-        ksplit = static_cast<int>(std::min<int64_t>(8, nsm / ntiles));
-        ksplit = std::min(ksplit, static_cast<int>(p.K / kSlabPos));  // at least one slab each
-        if (ksplit > 1) {
-            grid = static_cast<int>(ntiles) * ksplit;
-            box_rows = kTileM;
-        } else {
-            ksplit = 1;
-        }
-    }
+    const SpSplit plan = sp_plan(p, nsm);
+    if (plan.box_rows > kMaxRows) return cudaErrorNotSupported;
+    const int ksplit = plan.k;
+    const int64_t units = plan.units;  // row units: CTAs, or clusters with the split
+    const int grid = static_cast<int>(units) * ksplit;
+    const int box_rows = plan.box_rows;
     CUtensorMap tv, tm, tx;
     if (!encode2d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.values, Lv, p.rows, Lv * 2, 64,
                   box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1117,10 +1203,10 @@ cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta
     a.K = static_cast<int>(p.K);
     a.batch = p.batch;
     a.Np = Np;
-    // the boxes' row count (what each copy delivers); with the K split every
-    // CTA loads a full tile and takes its rows from the tile index
-    a.row_base = ksplit > 1 ? kTileM : static_cast<int>(p.rows / grid);
-    a.row_extra = ksplit > 1 ? 0 : static_cast<int>(p.rows % grid);
+    // rows spread evenly over the units (CTAs, or the tiles with the K
+    // split); a box carries row_base (+1) rows
+    a.row_base = static_cast<int>(p.rows / units);
+    a.row_extra = static_cast<int>(p.rows % units);
     a.y_f32 = p.y_f32 ? 1 : 0;
     a.idesc = spmm_tc_idesc(Np) | (1u << 2);  // sparse A
     a.desc_hi = desc_hi;
@@ -1155,7 +1241,7 @@ cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta
     if (avail <= 0) return cudaErrorInvalidDevice;
     // K split: rank 0 receives ranks 1..'s sums (4 KB each) in a region of
     // its own, which the ring never uses
-    const int part_bytes = ksplit > 1 ? (ksplit - 1) * kTileM * 32 : 0;
+    const int part_bytes = ksplit > 1 ? (ksplit - 1) * kTileM * a.ntile * 32 : 0;
     a.S = std::min(kSpMaxStages, (avail - tail - slack - part_bytes) / a.stage_bytes);
     if (bulk_tuning().sp_stages > 0) a.S = std::min(a.S, bulk_tuning().sp_stages);
     if (a.S < 2) return cudaErrorNotSupported;
@@ -1163,13 +1249,7 @@ cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta
     a.off_bar = a.off_part + part_bytes;
     a.err = p.err;
     const int smem = a.off_bar + tail;
-    static std::atomic<int> smem_set{0};
-    if (smem > smem_set.load(std::memory_order_relaxed)) {
-        cudaError_t e =
-            cudaFuncSetAttribute(nm_spmm_sp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        smem_set.store(smem, std::memory_order_relaxed);
-    }
+    if (!sp_allow_smem(avail)) return cudaErrorNotSupported;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kSpThreads);
@@ -1188,27 +1268,6 @@ cudaError_t launch_spmm_sp_impl(const SpmvProblem &p, uint64_t desc_hi, int meta
         attr[nattr].val.clusterDim.y = 1;
         attr[nattr].val.clusterDim.z = 1;
         ++nattr;
-        // a cluster of that size must fit on the device at this shared-memory
-        // size (cached per size and device), else no split
-        static std::atomic<int> fits[64][9];
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        int f = fits[dev][ksplit].load(std::memory_order_relaxed);
-        if (f == 0) {
-            cfg.attrs = attr;
-            cfg.numAttrs = nattr;
-            int nclusters = 0;
-            const cudaError_t e =
-                cudaOccupancyMaxActiveClusters(&nclusters, nm_spmm_sp_kernel, &cfg);
-            f = (e == cudaSuccess && nclusters > 0) ? 1 : -1;
-            if (e != cudaSuccess) cudaGetLastError();  // clear the sticky-free error state
-            fits[dev][ksplit].store(f, std::memory_order_relaxed);
-        }
-        if (f < 0) {
-            // relaunch without the split (rows evenly over the CTAs)
-            SpmvProblem q = p;
-            return launch_spmm_sp_nosplit(q, desc_hi, meta_mode, s);
-        }
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
