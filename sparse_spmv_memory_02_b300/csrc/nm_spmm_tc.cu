@@ -123,6 +123,17 @@ __device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *map, int x, 
         : "memory");
 }
 
+// As tma2d, with an L2 cache policy (createpolicy) for the bytes read.
+__device__ __forceinline__ void tma2d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                           uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // D[tmem_d] (+)= A[tmem_a] * B[b_desc]: A in tensor memory, B in shared memory.
 __device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)
@@ -714,6 +725,9 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         uint64_t *full = role == 0 ? fullv : role == 1 ? fullm : fullx;
         if (role == 2) pdl_wait();  // x may be the previous kernel's output
         if (lane == 0) {
+            // the weights are read once: evict them first, so that they do
+            // not push x (read by every CTA) out of L2
+            const uint64_t pol = l2_evict_first_policy();
             const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x) %
                               max(nslab, 1);
             const uint32_t box_rows = static_cast<uint32_t>(a.row_base + (a.row_extra ? 1 : 0));
@@ -740,9 +754,9 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 ks += slab_lo;
                 mbar_arrive_expect_tx(&full[s], tx);
                 if (role == 0) {
-                    tma2d(st, &tm_vals, ks * 64, r_begin, &full[s]);
+                    tma2d_hint(st, &tm_vals, ks * 64, r_begin, &full[s], pol);
                 } else if (role == 1) {
-                    tma2d(st + a.off_m, &tm_masks, ks * 4, r_begin, &full[s]);
+                    tma2d_hint(st + a.off_m, &tm_masks, ks * 4, r_begin, &full[s], pol);
                 } else if (a.x3d) {
                     tma3d(st + a.off_x, &tm_x, 0, 0, 2 * ks, &full[s]);
                 } else {
