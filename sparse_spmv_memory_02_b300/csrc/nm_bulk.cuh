@@ -303,6 +303,22 @@ struct BulkTuning {
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 
+// How the sparse-operand tensor-core product (nm_spmm_tc.cu) lays a 2:4
+// product over the SMs: without the split (k = 1) the rows are spread over
+// `units` CTAs; with it, `units` units of one or two 128-row tiles are each
+// shared by a cluster of k = 2, 4 or 8 CTAs, each streaming 1/k of K's
+// 128-position slabs.  box_rows: rows of the largest unit.
+struct SpSplit {
+    int k;
+    int64_t units;
+    int box_rows;
+};
+
+// The plan with the least estimated time (sp_split_plan in nm_bulk_plan.cu,
+// where the cost model is described).  resident[k] (k = 2, 4, 8): clusters
+// of k CTAs resident at once on the device (0: none).
+SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *resident);
+
 struct BulkPlan {
     int W, cpl, ktiles, tile_chunks, R, S, grid;
     int seg_v, seg_m, stage_bytes, off_bar, off_part, off_carry;

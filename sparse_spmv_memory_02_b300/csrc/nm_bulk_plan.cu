@@ -411,4 +411,59 @@ bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, 
     return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, max_warps, out, false, tab_bytes);
 }
 
+// The sparse-operand tensor-core product's plan.  Without the split the rows
+// are spread over min(rows, nsm) CTAs; with it, units of one or two 128-row
+// tiles are each shared by a cluster of k = 2, 4 or 8 CTAs (batch <= 8).
+// Measured on B300: a CTA's 128-position slab costs ~0.43 us with one tile
+// and ~0.61 us with two whatever rows they hold (below the HBM rate for
+// small tiles), a CTA streams at most ~55 GB/s and all of them ~6.2 TB/s;
+// the estimate of a plan is the largest of those bounds (weights at 1.125
+// bytes each), and the least estimate is taken, the smaller cluster within
+// 3 %.  Clusters of 3, 5, 6 or 7 are not used: the GPU held only ~40
+// clusters of 3 at once where the occupancy query promised 48, so part of
+// the grid ran in a second wave; a plan never has more units than clusters
+// of its size are resident.  Tuning keys: sp_split=0 (never split), sp_k
+// (only that cluster size, taken wherever it fits), sp_units (at least that
+// many units).
+SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *resident)
+{
+    constexpr int kTile = 128;  // rows of an MMA tile
+    constexpr int kSlab = 128;  // K positions of a slab
+    const int64_t nslab = K / kSlab;
+    const double bytes = static_cast<double>(rows) * static_cast<double>(K) * 1.125;
+    auto estimate = [&](int k, int64_t units, int box_rows) {
+        const int nt = (box_rows + kTile - 1) / kTile;
+        const double t_slab = static_cast<double>((nslab + k - 1) / k) * (nt == 1 ? 0.43 : 0.61);
+        const double ctas = static_cast<double>(units * k);
+        const double t_bw = std::max(bytes / 6.2e6, bytes / (ctas * 55e3));
+        return std::max(t_slab, t_bw);
+    };
+    SpSplit best;
+    best.k = 1;
+    best.units = std::max<int64_t>(1, std::min<int64_t>(rows, nsm));
+    best.box_rows = static_cast<int>((rows + best.units - 1) / best.units);
+    double t_best = estimate(1, best.units, best.box_rows);
+    const BulkTuning &tu = bulk_tuning();
+    if (!tu.sp_split || batch > 8 || rows < 1) return best;
+    for (int k = 2; k <= 8; k *= 2) {
+        if (tu.sp_k > 0 && k != tu.sp_k) continue;
+        if (k > nslab) break;
+        for (int nt = 1; nt <= 2; ++nt) {
+            int64_t units = (rows + kTile * nt - 1) / (kTile * nt);
+            if (tu.sp_units > 0) units = std::max<int64_t>(units, std::min<int64_t>(tu.sp_units, rows));
+            if (units * k > nsm || units > resident[k]) continue;
+            const int box_rows = static_cast<int>((rows + units - 1) / units);
+            if (box_rows > kTile * nt) continue;
+            const double t = estimate(k, units, box_rows);
+            if (t < 0.97 * t_best || (tu.sp_k > 0 && best.k == 1)) {
+                best.k = k;
+                best.units = units;
+                best.box_rows = box_rows;
+                t_best = t;
+            }
+        }
+    }
+    return best;
+}
+
 }  // namespace nm

@@ -1121,59 +1121,12 @@ int sp_resident_clusters(int k)
     return n;
 }
 
-struct SpSplit {
-    int k;           // CTAs a cluster (1: no split)
-    int64_t units;   // row units (CTAs without the split, clusters with it)
-    int box_rows;    // rows of the largest unit
-};
-
-// How the sparse kernel lays a product over the SMs.  Without the split the
-// rows are spread over min(rows, nsm) CTAs; with it, units of one or two
-// 128-row tiles are each shared by a cluster of k = 2, 4 or 8 CTAs, each
-// streaming 1/k of K's slabs.  Measured on B300: a CTA's slab costs ~0.43 us
-// with one tile and ~0.61 us with two whatever rows they hold (the MMA
-// pipeline's round trip, below the HBM rate for small tiles), and a CTA
-// streams at most ~55 GB/s, all of them ~6.2 TB/s; the plan with the least
-// estimated time is taken, the smaller cluster on a tie.  Clusters of 3, 5,
-// 6 or 7 are not used: the GPU held only ~40 clusters of 3 at once where the
-// occupancy query promised 48, so part of the grid ran in a second wave.
+// The split plan for this device: its resident cluster counts for k = 2, 4, 8.
 SpSplit sp_plan(const SpmvProblem &p, int nsm)
 {
-    const int64_t nslab = p.K / kSlabPos;
-    const double bytes = static_cast<double>(p.rows) * static_cast<double>(p.K) * 1.125;
-    auto estimate = [&](int k, int64_t units, int box_rows) {
-        const int nt = (box_rows + kTileM - 1) / kTileM;
-        const double t_slab = static_cast<double>((nslab + k - 1) / k) * (nt == 1 ? 0.43 : 0.61);
-        const double ctas = static_cast<double>(units * k);
-        const double t_bw = std::max(bytes / 6.2e6, bytes / (ctas * 55e3));
-        return std::max(t_slab, t_bw);
-    };
-    SpSplit best;
-    best.k = 1;
-    best.units = std::min<int64_t>(p.rows, nsm);
-    best.box_rows = static_cast<int>((p.rows + best.units - 1) / best.units);
-    double t_best = estimate(1, best.units, best.box_rows);
-    const BulkTuning &tu = bulk_tuning();
-    if (!tu.sp_split || p.batch > 8) return best;
-    for (int k = 2; k <= 8; k *= 2) {
-        if (tu.sp_k > 0 && k != tu.sp_k) continue;
-        if (k > nslab) break;
-        for (int nt = 1; nt <= 2; ++nt) {
-            int64_t units = (p.rows + kTileM * nt - 1) / (kTileM * nt);
-            if (tu.sp_units > 0) units = std::max<int64_t>(units, std::min<int64_t>(tu.sp_units, p.rows));
-            if (units * k > nsm || units > sp_resident_clusters(k)) continue;
-            const int box_rows = static_cast<int>((p.rows + units - 1) / units);
-            if (box_rows > kTileM * nt) continue;
-            const double t = estimate(k, units, box_rows);
-            if (t < 0.97 * t_best || (tu.sp_k > 0 && best.k == 1)) {
-                best.k = k;
-                best.units = units;
-                best.box_rows = box_rows;
-                t_best = t;
-            }
-        }
-    }
-    return best;
+    int resident[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    for (int k = 2; k <= 8; k *= 2) resident[k] = sp_resident_clusters(k);
+    return sp_split_plan(p.rows, p.K, p.batch, nsm, resident);
 }
 
 // The sparse-operand variant (nm_spmm_sp_kernel); same maps and conditions.

@@ -13,6 +13,8 @@
 //     at most one per row;
 //   * keep the per-lane partial sums (R rows x B vectors) within the
 //     kernel's register budget, and the carried partial sums within 64 KB.
+// The tensor-core product's K-split plans (sp_split_plan) are checked for
+// their limits too, and for the plans measured best on B300.
 #include <cstdint>
 #include <cstdio>
 #include <vector>
@@ -147,6 +149,39 @@ void group(const std::vector<int64_t> &rows, int64_t K, int N, int M, int B)
 
 }  // namespace
 
+// The tensor-core product's K-split plan for one shape: at most one CTA an
+// SM and one row a unit, no more units than clusters of that size are
+// resident, units of at most two 128-row tiles (one or two for a split),
+// every rank at least one 128-position slab, clusters of 2, 4 or 8 and only
+// up to 8 vectors.
+void sp_one(int64_t rows, int64_t K, int B, const int *resident, const char *dev)
+{
+    const nm::SpSplit p = nm::sp_split_plan(rows, K, B, kNsm, resident);
+    ++g_plans;
+    EXPECT(p.k == 1 || p.k == 2 || p.k == 4 || p.k == 8, "%s %lldx%lld B%d k %d", dev,
+           (long long)rows, (long long)K, B, p.k);
+    EXPECT(p.units >= 1 && p.units <= rows && p.units * p.k <= kNsm,
+           "%s %lldx%lld B%d units %lld k %d", dev, (long long)rows, (long long)K, B,
+           (long long)p.units, p.k);
+    EXPECT(p.box_rows == static_cast<int>((rows + p.units - 1) / p.units),
+           "%s %lldx%lld box %d", dev, (long long)rows, (long long)K, p.box_rows);
+    if (p.k > 1) {
+        EXPECT(B <= 8 && p.units <= resident[p.k] && p.k <= K / 128 && p.box_rows <= 256,
+               "%s %lldx%lld B%d split k %d units %lld box %d", dev, (long long)rows,
+               (long long)K, B, p.k, (long long)p.units, p.box_rows);
+    }
+}
+
+// Plans the B300 measurements chose (resident clusters of 2, 4, 8: 74, 37,
+// 18), at batch 8 with the default tuning.
+void sp_expect(int64_t rows, int64_t K, int k, int64_t units)
+{
+    const int resident[9] = {0, 0, 74, 0, 37, 0, 0, 0, 18};
+    const nm::SpSplit p = nm::sp_split_plan(rows, K, 8, kNsm, resident);
+    EXPECT(p.k == k && p.units == units, "%lldx%lld: plan k %d units %lld, expected k %d units %lld",
+           (long long)rows, (long long)K, p.k, (long long)p.units, k, (long long)units);
+}
+
 int main()
 {
     const int pats[][2] = {{2, 4}, {4, 8}, {1, 4}, {2, 8}, {1, 8}, {4, 4}, {8, 8}};
@@ -167,6 +202,26 @@ int main()
                 group(g, K, 2, 4, B);
                 group(g, K, 4, 8, B);
             }
+    // the tensor-core product's split plans, with the resident cluster counts
+    // measured on B300, fewer of them, and none (no split possible)
+    const int res_b300[9] = {0, 0, 74, 0, 37, 0, 0, 0, 18};
+    const int res_small[9] = {0, 0, 30, 0, 10, 0, 0, 0, 3};
+    const int res_none[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    for (int64_t r : rows_list)
+        for (int64_t K : {128L, 256L, 384L, 1024L, 4096L, 8192L, 25600L, 28672L})
+            for (int B : {1, 2, 3, 5, 8, 9, 16, 32}) {
+                sp_one(r, K, B, res_b300, "b300");
+                sp_one(r, K, B, res_small, "small");
+                sp_one(r, K, B, res_none, "none");
+            }
+    if (nm::bulk_tuning().sp_split && nm::bulk_tuning().sp_k == 0 &&
+        nm::bulk_tuning().sp_units == 0) {
+        sp_expect(8192, 28672, 4, 32);   // 32 two-tile units, clusters of 4
+        sp_expect(8192, 8192, 4, 32);
+        sp_expect(5120, 25600, 4, 20);
+        sp_expect(1024, 8192, 8, 8);     // 8 one-tile units, clusters of 8
+        sp_expect(28672, 8192, 1, 148);  // 194 rows a CTA, no split
+    }
     std::printf("%ld plans checked, %ld shapes without a row plan, %ld failures\n", g_plans,
                 g_none, g_fail);
     std::printf(g_fail ? "FAIL\n" : "OK\n");

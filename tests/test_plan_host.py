@@ -2,8 +2,9 @@
 tests/plan_host_check.cu with the library's planner (csrc/nm_bulk_plan.cu)
 for the host and runs it under the default tuning and the forced tunings the
 GPU tests use.  Every plan must fit shared memory, cover K and the rows
-exactly, keep regions 16-byte aligned and bound the partial sums.  No GPU is
-used."""
+exactly, keep regions 16-byte aligned and bound the partial sums; the
+tensor-core product's K-split plans must respect the SM count, the resident
+clusters and the tile sizes.  No GPU is used."""
 import os
 import shutil
 import subprocess
@@ -17,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 TUNINGS = ["", "rows_xtile=1024", "rows_task=512", "rows_R=4,rows_warps=3", "rows_ring=4096",
            "ctas=2", "rows_warps=1,rows_xtile=2048,rows_task=512", "rows_R=1",
-           "rows_xtile=4096,rows_task=1000,rows_pre=1"]
+           "rows_xtile=4096,rows_task=1000,rows_pre=1", "sp_split=0", "sp_k=2", "sp_k=8,sp_units=40"]
 
 
 @pytest.fixture(scope="module")
