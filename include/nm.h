@@ -55,8 +55,9 @@
 extern "C" {
 #endif
 
-#define NM_VERSION 160 /* 1.6.0 */
-#define NM_MAX_BATCH 8
+#define NM_VERSION 170 /* 1.7.0 */
+#define NM_MAX_BATCH 8     /* vectors a product takes on every path */
+#define NM_MAX_BATCH_TC 32 /* vectors a 2:4 product on the tensor cores takes */
 #define NM_MAX_GROUP 8
 
 /* A CUDA stream handle; identical to cudaStream_t. */
@@ -181,7 +182,11 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
 
 /*
  * The same product for 1 <= batch <= NM_MAX_BATCH vectors sharing one pass
- * over A (each weight byte is read once and used `batch` times).
+ * over A (each weight byte is read once and used `batch` times).  A 2:4
+ * matrix that the tensor-core path can run (below) takes up to
+ * NM_MAX_BATCH_TC vectors; above NM_MAX_BATCH any other matrix returns
+ * NM_ERR_UNSUPPORTED (as does NM_BULK_TUNE=tc=0), and a batch outside
+ * [1, NM_MAX_BATCH_TC] NM_ERR_INVALID_ARG.
  *   x  fp16 [batch][ldx], device; ldx >= K; with batch > 1, ldx must be a
  *      multiple of 8 so that every vector starts 16-byte aligned.
  *   y  y_type [batch][ldy], device; ldy >= rows.  Row b of y receives A x_b.
@@ -189,9 +194,10 @@ nm_status nm_spmv(const nm_matrix *A, const void *x, void *y, nm_dtype y_type,
  * 128, at most 256 rows per SM and x and the packed arrays 16-byte aligned
  * is multiplied on the tensor cores when that is faster: from batch 5 on
  * layers of at least 4 Mi weights (rows x K), at batch 3-4 above 24 M, at
- * batch 2 from 128 Mi with at most 128 rows per SM.  Layers of at most one
+ * batch 2 from 128 Mi with at most 128 rows per SM, and always above
+ * NM_MAX_BATCH.  Layers of at most one
  * 128-row tile per SM then split K over thread-block clusters of 2, 4 or 8
- * CTAs (batch <= 8).  The packed values are then the compressed operand of the
+ * CTAs.  The packed values are then the compressed operand of the
  * sparse tensor-core MMA (the mask bits become its metadata on chip) and
  * products are summed with fp32 accumulation in another order, within the
  * same error bound and deterministic from call to call; that path overlaps
@@ -220,8 +226,10 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
  * the matrix); matrices that differ in N, M or K are NM_ERR_INVALID_ARG.
  * When the shapes cannot share a launch, or every product takes the
  * tensor-core path of nm_spmv_batched, the products are launched one by one,
- * with the same results (then each on the kernel nm_spmv_batched picks).  Asynchronous, allocates nothing, may be
- * captured in a CUDA graph; the products' y must not overlap.
+ * with the same results (then each on the kernel nm_spmv_batched picks); a
+ * batch above NM_MAX_BATCH needs every product to take that path.
+ * Asynchronous, allocates nothing, may be captured in a CUDA graph; the
+ * products' y must not overlap.
  */
 nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int64_t ldx,
                         void *const *y, const int64_t *ldy, int batch, nm_dtype y_type,
@@ -297,7 +305,8 @@ nm_status nm_prune_pack(const void *W, const float *col_scale, int64_t rows, int
  *   x         fp16 [batch][ldx], device (as nm_spmv_batched).
  *   h         h_type [batch][ldh], device; ldh >= rows.
  * Both dot products are carried in fp32 as by nm_spmv; silu and the product
- * are evaluated in fp32 and h is rounded once.  Errors as nm_spmv_batched;
+ * are evaluated in fp32 and h is rounded once.  Errors as nm_spmv_batched
+ * (batch at most NM_MAX_BATCH: a larger one is NM_ERR_UNSUPPORTED);
  * in addition NM_ERR_INVALID_ARG if gate and up differ in shape, and
  * NM_ERR_UNSUPPORTED unless K is a multiple of 128 and 8 % N == 0 (the
  * shapes the streaming kernel takes).  Asynchronous, allocates nothing, may

@@ -167,6 +167,8 @@ nm_status check_matrix(const nm_matrix *A)
     return NM_OK;
 }
 
+bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc);
+
 // Checks the arguments of one product y = A x (batch vectors) and fills `p`.
 // Sets *empty, having done the whole job, when rows == 0 (nothing to do) or
 // K == 0 (y is zeroed on `s`).
@@ -177,8 +179,14 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
     *empty = false;
     nm_status st = check_matrix(A);
     if (st != NM_OK) return st;
-    if (batch < 1 || batch > NM_MAX_BATCH)
-        return fail(NM_ERR_INVALID_ARG, "batch=%d outside [1, %d]", batch, NM_MAX_BATCH);
+    if (batch < 1 || batch > NM_MAX_BATCH_TC)
+        return fail(NM_ERR_INVALID_ARG, "batch=%d outside [1, %d]", batch, NM_MAX_BATCH_TC);
+    // more than NM_MAX_BATCH vectors: only the 2:4 tensor-core product (the
+    // rest of its conditions is checked below, once the device is known)
+    if (batch > NM_MAX_BATCH && !(A->N == 2 && A->M == 4 && A->K % 128 == 0))
+        return fail(NM_ERR_UNSUPPORTED,
+                    "batch=%d > %d needs a 2:4 matrix with K a multiple of 128 (the tensor-core "
+                    "path)", batch, NM_MAX_BATCH);
     if (y_type != NM_F16 && y_type != NM_F32)
         return fail(NM_ERR_INVALID_ARG, "unknown y_type %d", (int)y_type);
     const size_t esize = y_type == NM_F32 ? 4 : 2;
@@ -221,6 +229,14 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
     p->ldy = ldy;
     p->batch = batch;
     p->y_f32 = y_type == NM_F32;
+    if (batch > NM_MAX_BATCH) {
+        uint32_t lbo = 0;
+        if (!takes_tensor_cores(*p, &lbo))
+            return fail(NM_ERR_UNSUPPORTED,
+                        "batch=%d > %d: the tensor-core path does not apply (at most 256 rows "
+                        "per SM, x, values and masks 16-byte aligned, not turned off)",
+                        batch, NM_MAX_BATCH);
+    }
     cudaError_t e = device_error_word(&p->err);
     if (e != cudaSuccess) return cuda_fail(e, "nm_spmv: device error word");
     return NM_OK;
@@ -245,7 +261,7 @@ bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
     const int tc = nm::spmm_tc_mode(lbo_enc);
     const int nsm = nm::sm_count();
     if (tc == 0 || nsm <= 0 || !nm::spmm_tc_applies(p, nsm)) return false;
-    if (tc == 1) return true;
+    if (tc == 1 || p.batch > NM_MAX_BATCH) return true;
     const int64_t weights = p.rows * p.K;
     const int64_t per_sm = (p.rows + nsm - 1) / nsm;
     if (p.batch >= 5) return weights >= (4ll << 20);
@@ -260,6 +276,8 @@ nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)
     uint32_t tc_lbo = 0;
     if (takes_tensor_cores(p, &tc_lbo))
         e = nm::launch_spmm_tc(p, nm::spmm_tc_desc_hi(tc_lbo), s);
+    if (e == cudaErrorNotSupported && p.batch > NM_MAX_BATCH)  // no other kernel takes it
+        return fail(NM_ERR_UNSUPPORTED, "batch=%d: no tensor-core plan fits", p.batch);
     if (e == cudaErrorNotSupported && nm::bulk_path_applies(p.N, p.M, p.K)) {
         nm::SpmvGroup g;
         g.count = 1;
@@ -452,6 +470,9 @@ nm_status nm_spmv_gate_up_silu(const nm_matrix *gate, const nm_matrix *up, const
         return fail(NM_ERR_INVALID_ARG, "gate and up must have the same rows, K, N and M");
     nm_status st = check_matrix(gate);
     if (st != NM_OK) return st;
+    if (batch > NM_MAX_BATCH && batch <= NM_MAX_BATCH_TC)
+        return fail(NM_ERR_UNSUPPORTED, "nm_spmv_gate_up_silu: batch=%d > %d", batch,
+                    NM_MAX_BATCH);
     if (gate->rows > 0 && gate->K > 0 && !nm::bulk_path_applies(gate->N, gate->M, gate->K))
         return fail(NM_ERR_UNSUPPORTED,
                     "nm_spmv_gate_up_silu: K must be a multiple of 128 and N:M one of 1:4, "

@@ -413,7 +413,9 @@ bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, 
 
 // The sparse-operand tensor-core product's plan.  Without the split the rows
 // are spread over min(rows, nsm) CTAs; with it, units of one or two 128-row
-// tiles are each shared by a cluster of k = 2, 4 or 8 CTAs (batch <= 8).
+// tiles are each shared by a cluster of k = 2, 4 or 8 CTAs (rank 0 receives
+// the other ranks' sums, 8, 16 or 32 floats a row by the batch, in at most
+// 64 KB of shared memory).
 // Measured on B300: a CTA's 128-position slab costs ~0.43 us with one tile
 // and ~0.61 us with two whatever rows they hold (below the HBM rate for
 // small tiles), a CTA streams at most ~55 GB/s and all of them ~6.2 TB/s;
@@ -444,7 +446,8 @@ SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *re
     best.box_rows = static_cast<int>((rows + best.units - 1) / best.units);
     double t_best = estimate(1, best.units, best.box_rows);
     const BulkTuning &tu = bulk_tuning();
-    if (!tu.sp_split || batch > 8 || rows < 1) return best;
+    if (!tu.sp_split || batch > 32 || rows < 1) return best;
+    const int row_bytes = batch <= 8 ? 32 : batch <= 16 ? 64 : 128;  // a rank's sums of a row
     for (int k = 2; k <= 8; k *= 2) {
         if (tu.sp_k > 0 && k != tu.sp_k) continue;
         if (k > nslab) break;
@@ -452,6 +455,8 @@ SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *re
             int64_t units = (rows + kTile * nt - 1) / (kTile * nt);
             if (tu.sp_units > 0) units = std::max<int64_t>(units, std::min<int64_t>(tu.sp_units, rows));
             if (units * k > nsm || units > resident[k]) continue;
+            // rank 0's region for the other ranks' sums stays within 64 KB
+            if ((k - 1) * kTile * nt * row_bytes > 65536) continue;
             const int box_rows = static_cast<int>((rows + units - 1) / units);
             if (box_rows > kTile * nt) continue;
             const double t = estimate(k, units, box_rows);

@@ -524,7 +524,8 @@ struct SpArgs {
     int meta_mode;            // sp_meta_word mode
     int ksplit;               // CTAs (one cluster) sharing a unit of rows, each a part of K
                               // (1: no split, rows split evenly over the CTAs)
-    int off_part;             // K split: rank 0's region for ranks 1..'s sums, [r - 1][row][8]
+    int off_part;             // K split: rank 0's region for ranks 1..'s sums, [r - 1][row][cols]
+    int split_cols;           // K split: columns summed across the cluster (8, 16 or 32 >= batch)
     uint32_t tmem_cols;       // tensor-memory columns allocated (256 or 512)
     int spin;                 // 1: metadata warps and MMA issuers spin on their barriers
     int meta_sel;             // 1: an MMA's metadata word is column kk of the buffer's
@@ -625,9 +626,11 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
         sp_meta_col(a.meta_base, a.ntile, a.nmbuf - 1, a.ntile - 1, 3) >= a.tmem_cols ||
         (a.ksplit > 1 &&
          (a.ksplit > 8 || gridDim.x % a.ksplit != 0 ||
-          a.row_base + (a.row_extra ? 1 : 0) > kTileM * a.ntile || a.Np != 16 ||
+          a.row_base + (a.row_extra ? 1 : 0) > kTileM * a.ntile ||
+          (a.split_cols != 8 && a.split_cols != 16 && a.split_cols != 32) ||
+          a.batch > a.split_cols || a.split_cols > a.Np ||
           a.K / kSlabPos < a.ksplit || (a.off_part & 15) ||
-          a.off_part + (a.ksplit - 1) * kTileM * a.ntile * 32 > a.off_bar))) {
+          a.off_part + (a.ksplit - 1) * kTileM * a.ntile * a.split_cols * 4 > a.off_bar))) {
         if (threadIdx.x == 0) atomicOr(a.err, kDevErrSmemAlign);
         return;
     }
@@ -687,10 +690,12 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
             *failed = 0;
         }
         mbar_fence_init();
-        // rank 0 of a split expects ranks 1..'s sums: 32 bytes for each row
-        // of its tiles (the ranks of a cluster share the unit, so its tiles)
+        // rank 0 of a split expects ranks 1..'s sums: split_cols floats for
+        // each row of its tiles (the ranks of a cluster share the unit, so
+        // its tiles)
         if (i == 0 && a.ksplit > 1 && rank == 0)
-            mbar_arrive_expect_tx(part, static_cast<uint32_t>((a.ksplit - 1) * nconv * 32 * 32));
+            mbar_arrive_expect_tx(
+                part, static_cast<uint32_t>((a.ksplit - 1) * nconv * 32 * a.split_cols * 4));
     }
     // the cluster's barriers are initialised before any CTA of it writes to
     // another (the matching wait is in the epilogue)
@@ -894,52 +899,61 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     pdl_wait();  // y may still be read by the previous kernel
     if (a.ksplit > 1) {
-        // K split (batch <= 8, so Np = 16 and 8 columns matter): ranks 1..
-        // send their sums to rank 0's region with st.async, which counts them
-        // on rank 0's `part` barrier; rank 0 adds them in rank order.  Every
-        // rank sends (zeros after a failure) so that rank 0's wait always
-        // ends; the cluster wait makes rank 0's barrier initialisation
-        // visible first.
+        // K split (split_cols = 8, 16 or 32 columns matter, at least the
+        // batch): ranks 1.. send their sums to rank 0's region with
+        // st.async, which counts them on rank 0's `part` barrier; rank 0 adds
+        // them in rank order.  Every rank sends (zeros after a failure) so
+        // that rank 0's wait always ends; the cluster wait makes rank 0's
+        // barrier initialisation visible first.
         cluster_wait();
         if (warp < nconv) {
             const int t = warp >> 2, q = warp & 3;
             const int row = t * kTileM + 32 * q + lane;  // row in the unit
-            float v[8];
+            const int ncol = a.split_cols;
+            float v[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.f;
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
             if (go) {
                 // the tile's sets that slabs started (issuer i, set j at
                 // (i * nacc + j) * 16; issuers 2t, 2t + 1 with two tiles, else
-                // all four): up to 4 a batch, one wait each
+                // all four), 8 columns at a time: up to 4 sets a batch, one
+                // wait each
                 const int i0 = ntile == 2 ? 2 * t : 0;
                 const int ni = ntile == 2 ? 2 : kSpMmaWarps;
                 const int nused = min(a.nacc, nslab);
                 const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * q) << 16);
-                for (int i = i0; i < i0 + ni; ++i)
-                    for (int j0 = 0; j0 < nused; j0 += 4) {
-                        uint32_t r[4][8];
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            if (j0 + jj < nused)
-                                tmem_ld8_nowait(lanes + (i * a.nacc + j0 + jj) * a.Np, r[jj]);
-                        tmem_wait_ld();
+                for (int h = 0; h < 4; ++h) {
+                    if (8 * h >= ncol) break;
+                    for (int i = i0; i < i0 + ni; ++i)
+                        for (int j0 = 0; j0 < nused; j0 += 4) {
+                            uint32_t r[4][8];
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            if (j0 + jj < nused)
+                            for (int jj = 0; jj < 4; ++jj)
+                                if (j0 + jj < nused)
+                                    tmem_ld8_nowait(lanes + (i * a.nacc + j0 + jj) * a.Np + 8 * h,
+                                                    r[jj]);
+                            tmem_wait_ld();
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) v[c] += __uint_as_float(r[jj][c]);
-                    }
+                            for (int jj = 0; jj < 4; ++jj)
+                                if (j0 + jj < nused)
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c)
+                                        v[8 * h + c] += __uint_as_float(r[jj][c]);
+                        }
+                }
             }
-            // rank r's sums at [r - 1][row] in rows of 32 bytes, kTileM * a.ntile
-            // rows a rank
+            // rank r's sums at [r - 1][row] in rows of ncol floats, kTileM *
+            // a.ntile rows a rank
             const int rank_rows = kTileM * a.ntile;
             const uint32_t my_part = smem_addr(smem + a.off_part);
             if (rank > 0) {
                 const uint32_t dst = cluster_map(
-                    my_part + static_cast<uint32_t>(((rank - 1) * rank_rows + row) * 32), 0);
+                    my_part + static_cast<uint32_t>(((rank - 1) * rank_rows + row) * ncol * 4), 0);
                 const uint32_t bar = cluster_map(smem_addr(part), 0);
-                st_async_v4(dst, v[0], v[1], v[2], v[3], bar);
-                st_async_v4(dst + 16, v[4], v[5], v[6], v[7], bar);
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    if (c < ncol) st_async_v4(dst + 4 * c, v[c], v[c + 1], v[c + 2], v[c + 3], bar);
             } else {
                 // ranks 1.. reach this point within their own bounded waits
                 bool landed = true;
@@ -948,15 +962,20 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 if (!landed && lane == 0) atomicOr(a.err, kDevErrPipeTimeout);
                 const float *pp = reinterpret_cast<const float *>(smem + a.off_part);
                 for (int r = 1; r < a.ksplit; ++r) {
-                    const float *src = pp + ((r - 1) * rank_rows + row) * 8;
-                    const float4 p0 = *reinterpret_cast<const float4 *>(src);
-                    const float4 p1 = *reinterpret_cast<const float4 *>(src + 4);
-                    v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-                    v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+                    const float *src = pp + ((r - 1) * rank_rows + row) * ncol;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        if (c < ncol) {
+                            const float4 pv = *reinterpret_cast<const float4 *>(src + c);
+                            v[c] += pv.x;
+                            v[c + 1] += pv.y;
+                            v[c + 2] += pv.z;
+                            v[c + 3] += pv.w;
+                        }
                 }
                 if (go && landed && row < r_count) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < 32; ++j)
                         if (j < a.batch) store_y(a.y, j * a.ldy + r_begin + row, v[j], a.y_f32 != 0);
                 }
             }
@@ -1208,7 +1227,8 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     if (avail <= 0) return cudaErrorInvalidDevice;
     // K split: rank 0 receives ranks 1..'s sums (4 KB each) in a region of
     // its own, which the ring never uses
-    const int part_bytes = ksplit > 1 ? (ksplit - 1) * kTileM * a.ntile * 32 : 0;
+    a.split_cols = p.batch <= 8 ? 8 : p.batch <= 16 ? 16 : 32;
+    const int part_bytes = ksplit > 1 ? (ksplit - 1) * kTileM * a.ntile * a.split_cols * 4 : 0;
     a.S = std::min(kSpMaxStages, (avail - tail - slack - part_bytes) / a.stage_bytes);
     if (bulk_tuning().sp_stages > 0) a.S = std::min(a.S, bulk_tuning().sp_stages);
     if (a.S < 2) return cudaErrorNotSupported;

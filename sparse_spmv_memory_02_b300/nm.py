@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libnm.so")
 NM_OK, NM_ERR_INVALID_ARG, NM_ERR_UNSUPPORTED, NM_ERR_BAD_MASK, NM_ERR_CUDA = 0, 1, 2, 3, 4
 NM_F16, NM_F32 = 0, 1
 NM_MAX_BATCH = 8
+NM_MAX_BATCH_TC = 32
 NM_MAX_GROUP = 8
 
 

@@ -152,8 +152,8 @@ void group(const std::vector<int64_t> &rows, int64_t K, int N, int M, int B)
 // The tensor-core product's K-split plan for one shape: at most one CTA an
 // SM and one row a unit, no more units than clusters of that size are
 // resident, units of at most two 128-row tiles (one or two for a split),
-// every rank at least one 128-position slab, clusters of 2, 4 or 8 and only
-// up to 8 vectors.
+// every rank at least one 128-position slab, clusters of 2, 4 or 8, at most
+// 32 vectors and rank 0's region for the other ranks' sums within 64 KB.
 void sp_one(int64_t rows, int64_t K, int B, const int *resident, const char *dev)
 {
     const nm::SpSplit p = nm::sp_split_plan(rows, K, B, kNsm, resident);
@@ -166,7 +166,9 @@ void sp_one(int64_t rows, int64_t K, int B, const int *resident, const char *dev
     EXPECT(p.box_rows == static_cast<int>((rows + p.units - 1) / p.units),
            "%s %lldx%lld box %d", dev, (long long)rows, (long long)K, p.box_rows);
     if (p.k > 1) {
-        EXPECT(B <= 8 && p.units <= resident[p.k] && p.k <= K / 128 && p.box_rows <= 256,
+        const int nt = (p.box_rows + 127) / 128;
+        EXPECT(B <= 32 && p.units <= resident[p.k] && p.k <= K / 128 && p.box_rows <= 256 &&
+                   (p.k - 1) * 128 * nt * (B <= 8 ? 32 : B <= 16 ? 64 : 128) <= 65536,
                "%s %lldx%lld B%d split k %d units %lld box %d", dev, (long long)rows,
                (long long)K, B, p.k, (long long)p.units, p.box_rows);
     }

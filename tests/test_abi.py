@@ -64,7 +64,8 @@ def test_spmv_group_checks_arguments_on_the_host():
     assert L.nm_spmv_group(None, 1, xp, 128, yp, None, 1, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
     same = (nm.nm_matrix * 2)(A, A)
     # per-matrix checks name the matrix: batch out of range
-    assert L.nm_spmv_group(same, 2, xp, 64, yp, None, 9, nm.NM_F16, None) == nm.NM_ERR_INVALID_ARG
+    assert L.nm_spmv_group(same, 2, xp, 64, yp, None, nm.NM_MAX_BATCH_TC + 1, nm.NM_F16,
+                           None) == nm.NM_ERR_INVALID_ARG
     assert nm.nm_last_error().startswith("matrix 0")
     # misaligned x of the second matrix
     xbad = (ctypes.c_void_p * 2)(C16, C16 + 2)
@@ -184,7 +185,7 @@ def _spmv_b(mat, x=C16, ldx=None, y=D16, ldy=None, batch=1, yt=nm.NM_F16):
 
 @pytest.mark.parametrize("kwargs,status", [
     (dict(batch=0), nm.NM_ERR_INVALID_ARG),
-    (dict(batch=9), nm.NM_ERR_INVALID_ARG),
+    (dict(batch=nm.NM_MAX_BATCH_TC + 1), nm.NM_ERR_INVALID_ARG),
     (dict(yt=7), nm.NM_ERR_INVALID_ARG),
     (dict(ldx=255), nm.NM_ERR_INVALID_ARG),
     (dict(ldy=63), nm.NM_ERR_INVALID_ARG),
@@ -198,6 +199,15 @@ def _spmv_b(mat, x=C16, ldx=None, y=D16, ldy=None, batch=1, yt=nm.NM_F16):
 def test_spmv_batched_rejects_bad_arguments(kwargs, status):
     assert _spmv_b(_mat(), **kwargs) == status
     assert nm.nm_last_error() != ""
+
+
+@pytest.mark.parametrize("N,M,K", [(4, 8, 256), (1, 4, 256), (2, 8, 256), (2, 4, 192)])
+def test_batch_above_8_needs_the_tensor_core_path(N, M, K):
+    """Above NM_MAX_BATCH only 2:4 products with K a multiple of 128 run (on
+    the tensor cores): any other pattern or K is refused on the host."""
+    st = _spmv_b(_mat(K=K, N=N, M=M), ldx=K + (-K) % 8, batch=nm.NM_MAX_BATCH + 1)
+    assert st == nm.NM_ERR_UNSUPPORTED
+    assert "tensor-core" in nm.nm_last_error()
 
 
 @pytest.mark.parametrize("mat,status", [
@@ -260,7 +270,7 @@ def test_binding_constants_match_the_header():
     defines = {k: int(v.rstrip("uUlL"), 0)
                for k, v in re.findall(r"#define (NM_\w+) (0x[0-9a-fA-F]+|\d+)[uUlL]*", text)}
     mirrored = [k for k in defines if hasattr(nm, k)]
-    assert {"NM_MAX_BATCH", "NM_MAX_GROUP", "NM_DEVERR_PIPE_TIMEOUT",
+    assert {"NM_MAX_BATCH", "NM_MAX_BATCH_TC", "NM_MAX_GROUP", "NM_DEVERR_PIPE_TIMEOUT",
             "NM_DEVERR_SMEM_ALIGN"} <= set(mirrored), mirrored
     for k in mirrored:
         assert getattr(nm, k) == defines[k], k

@@ -83,6 +83,13 @@ CASES = [
     (1000, 640, 3, True, False),      # clusters of 5; last tile 104 rows
     (4100, 1152, 8, False, True),     # clusters of 4 over 9 slabs (3, 2, 2, 2)
     (8192, 1024, 1, False, True),     # batch 1, clusters of 2
+    # more than 8 vectors (the tensor-core path only): 16-column split sums
+    # up to batch 16, then N = 32 MMAs without the split
+    (1000, 896, 12, True, True),
+    (8192, 1024, 16, False, False),
+    (149, 1024, 9, False, True),
+    (4096, 4096, 24, True, True),
+    (28672, 512, 32, False, True),    # two tiles a CTA, N = 32
 ]
 
 
@@ -98,6 +105,44 @@ def test_tensor_core_path_forced(tune):
     assert r.returncode == 0, r.stderr[-2000:]
     out = json.loads(r.stdout.strip().splitlines()[-1])
     assert out["fails"] == [] and out["errors"] == 0, out
+
+
+@pytest.mark.parametrize("rows,K,B", [(28672, 8192, 16), (8192, 8192, 16), (8192, 4096, 32)])
+def test_tensor_core_path_above_batch_8(rows, K, B):
+    """Above 8 vectors only the tensor-core path runs: sampled rows of the
+    70B-shaped gate and of split layers against the oracle, at batch 16 (the
+    16-column split sums) and 32 (N = 32 MMAs)."""
+    W = nm_synth.weights(rows, K, 90 + B, DEV)
+    mask = nm_synth.topn_mask(W, 2, 4)
+    A = nm.nm_pack(W, mask, 2, 4)
+    x = nm_synth.activations(K, B, 91 + B, True, DEV)
+    y = nm.nm_spmv_batched(A, x, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(B)
+    pick = np.sort(g.choice(rows, 256, replace=False))
+    idx = torch.from_numpy(pick).to(DEV)
+    yr, sr = oracle.spmv_dense(W[idx].cpu().numpy().view(np.uint16), mask[idx].cpu().numpy(),
+                               x.cpu().numpy().view(np.uint16))
+    ok = oracle.within_tolerance(y[:, idx].double().cpu().numpy(), yr, sr)
+    assert ok.all(), "%d/%d outside tolerance" % ((~ok).sum(), ok.size)
+    assert nm.nm_device_errors() == 0
+
+
+def test_batch_above_8_unsupported_where_the_tensor_cores_cannot_run():
+    """257 rows per SM exceed the tensor-core product's two tiles: batch 9
+    is refused (NM_ERR_UNSUPPORTED) before any launch, batch 8 runs on the
+    CUDA cores."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, K = 257 * nsm, 256
+    W = nm_synth.weights(rows, K, 5, DEV)
+    A = nm.nm_pack(W, nm_synth.topn_mask(W, 2, 4), 2, 4)
+    x = nm_synth.activations(K, 9, 6, True, DEV)
+    with pytest.raises(nm.NMError) as e:
+        nm.nm_spmv_batched(A, x)
+    assert e.value.status == nm.NM_ERR_UNSUPPORTED
+    y = nm.nm_spmv_batched(A, x[:8])
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
 
 
 def test_tensor_core_path_default_on_70b_gate_batch8():
