@@ -535,9 +535,9 @@ nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int
         }
         ++g.count;
     }
-    // members that all take the tensor-core product (the 70B-shaped gate/up
-    // at batch 8) run as separate launches of it, faster than one fused
-    // CUDA-core launch
+    // members that all take the tensor-core product (e.g. the 70B-shaped
+    // gate/up from batch 3) run as separate launches of it, faster than one
+    // fused CUDA-core launch (and above 8 vectors the only way)
     bool all_tc = g.count > 0;
     for (int i = 0; i < g.count && all_tc; ++i) {
         uint32_t lbo = 0;

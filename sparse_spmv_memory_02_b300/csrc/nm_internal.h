@@ -88,8 +88,8 @@ bool spmm_tc_applies(const SpmvProblem &p, int nsm);
 cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s);
 uint32_t spmm_tc_idesc(int N);
 // When products take that path (tuning key tc: 1 wherever it applies, 0
-// never, -1 at batch 8 with more than 128 rows a CTA) and its descriptors'
-// encoded leading-byte-offset field (tuning key tc_lbo).
+// never, -1 by batch and layer size: takes_tensor_cores in nm_api.cu) and
+// its descriptors' encoded leading-byte-offset field (tuning key tc_lbo).
 int spmm_tc_mode(uint32_t *lbo_enc);
 uint64_t spmm_tc_desc_hi(uint32_t lbo_enc);
 

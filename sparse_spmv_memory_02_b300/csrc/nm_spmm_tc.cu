@@ -1,15 +1,18 @@
-// 2:4 sparse x dense product for batches of 8 to 32 vectors on the
-// fifth-generation tensor cores (tcgen05), for sm_103a.  The library calls
-// it at batch 8 (its largest batch) for 2:4 layers with more than 128 rows
-// per SM, where it is faster than the CUDA-core row kernel.
+// 2:4 sparse x dense products for 2 to 32 vectors on the fifth-generation
+// tensor cores (tcgen05), for sm_103a.  The library routes a 2:4 product
+// here where that is faster than the CUDA-core row kernel (from batch 2-5 by
+// layer size, takes_tensor_cores in nm_api.cu) and for every batch above 8.
 //
 // The same N:M product as the streaming kernels ("SparseDecoding:
 // Decoding-Aware Pruning for Accurate and Efficient LLM Inference",
 // Abstract: bitmask indexing, fixed-step traversal), for the regime where
-// the batch makes the CUDA-core kernel instruction-bound (8 x 8 products and
+// the batch makes the CUDA-core kernel instruction-bound (8 x B products and
 // their x gathers per 16-byte chunk): the packed weights are still streamed
-// from HBM exactly once, but each CTA expands its rows to dense fp16 in
-// tensor memory and the tensor cores do the multiply.
+// from HBM exactly once and the tensor cores do the multiply.  Two kernels:
+// nm_spmm_sp_kernel (the default, further below) takes the packed values as
+// the sparse A operand of tcgen05.mma.sp; nm_spmm_tc_kernel (tuning key
+// tc_sp=0, described here) expands each CTA's rows to dense fp16 in tensor
+// memory first.
 //
 //   * One CTA per SM, rows split evenly over the CTAs (at most 256 rows a
 //     CTA: two 128-row MMA tiles, the second possibly partial).
