@@ -268,6 +268,7 @@ struct BulkTuning {
     int rows_xtile_bytes = 49152;  // largest x tile (B vectors) before K is tiled
     int rows_pair = 0;             // size each CTA to half an SM (see nm_rows.cuh)
     int rows_pre = 1;              // tasks per warp copied before the dependence wait (<= SW)
+    int rows_prew = 16;            // warps of a CTA that copy them (the first ones)
     int rows_two = -1;             // 1: two rows a task (segments too) at batch <= 2 for
                                    // patterns whose chunk spans 32 positions; 0: never; -1: auto
     int rows_l2pre_bytes = 0;      // weight bytes per CTA warmed in L2 before that wait
@@ -297,7 +298,7 @@ struct BulkTuning {
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
-// rows_ring, rows_xtile, rows_pair, rows_pre, rows_l2pre, rows_two, rows (row-per-warp kernel),
+// rows_ring, rows_xtile, rows_pair, rows_pre, rows_prew, rows_l2pre, rows_two, rows (row-per-warp kernel),
 // ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs, sp_sel, sp_spin, sp_split,
 // sp_stages, sp_tmem, sp_k, sp_units
 // (both), tc, tc_lbo (tensor-core product); read once per process.

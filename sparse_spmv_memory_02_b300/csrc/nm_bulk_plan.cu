@@ -44,6 +44,7 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "rows") && (v == 0 || v == 1)) t.rows_kernel = v;
         else if (!std::strcmp(tok, "rows_pair") && (v == 0 || v == 1)) t.rows_pair = v;
         else if (!std::strcmp(tok, "rows_pre") && v >= 0 && v <= 8) t.rows_pre = v;
+        else if (!std::strcmp(tok, "rows_prew") && v >= 0 && v <= 16) t.rows_prew = v;
         else if (!std::strcmp(tok, "rows_two") && v >= -1 && v <= 1) t.rows_two = v;
         else if (!std::strcmp(tok, "wait_fault_test") && (v == 0 || v == 1)) t.wait_fault_test = v;
         else if (!std::strcmp(tok, "tc_sp") && (v == 0 || v == 1)) t.tc_sp = v;

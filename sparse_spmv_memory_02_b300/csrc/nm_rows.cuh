@@ -91,6 +91,7 @@ struct RowsArgs {
     int nmat;
     int SW;                 // slots per warp
     int pre;                // tasks per warp issued before the dependence wait (<= SW)
+    int pre_warps;          // warps that issue them (the first pre_warps of the CTA)
     int chunks;             // 16-byte value chunks per row
     int tile_chunks;        // chunks per K tile (the x held in shared memory at once)
     int ktiles;
@@ -251,7 +252,7 @@ nm_spmv_rows_kernel(const __grid_constant__ RowsArgs a)
 
     // This warp's first `pre` tasks (weights only: no dependence on the
     // previous kernel); the rest of its first SW after x is staged.
-    if (lane == 0)
+    if (lane == 0 && warp < a.pre_warps)
         while (issued < a.pre && issued < ncopy)
             issue_next(my_ring + static_cast<size_t>(issued) * a.stage_bytes, &my_full[issued]);
 
@@ -554,6 +555,7 @@ cudaError_t launch_rows_instance(const SpmvGroup &g, const RowsPlan &pl, const i
     a.nseg_last = pl.nseg_last;
     a.SW = pl.SW;
     a.pre = std::min(bulk_tuning().rows_pre, pl.SW);
+    a.pre_warps = bulk_tuning().rows_prew;
     // L2 warm-up only where the CTA consumes its rows in address order (one K tile)
     a.l2pre_rows = pl.ktiles == 1 ? static_cast<int>(bulk_tuning().rows_l2pre_bytes /
                                                      (a.vrow_bytes + a.mrow_bytes))
