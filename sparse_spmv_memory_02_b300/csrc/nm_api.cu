@@ -256,11 +256,13 @@ nm_status prepare_product(const nm_matrix *A, const void *x, int64_t ldx, void *
 // 1024 x 8192 stay on the row kernel); at batch 2 only on the largest split
 // layers (8192 x 28672: 43 against 58 us; 8192 x 8192 is a tie, 28672 x
 // 8192 slightly slower).  Tuning key tc forces it on (1) or off (0).
-bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
+// The rule alone, for a product (or a group, p.rows its rows together) that
+// the tensor-core product can run.
+bool takes_tensor_cores_rule(const nm::SpmvProblem &p, uint32_t *lbo_enc)
 {
     const int tc = nm::spmm_tc_mode(lbo_enc);
     const int nsm = nm::sm_count();
-    if (tc == 0 || nsm <= 0 || !nm::spmm_tc_applies(p, nsm)) return false;
+    if (tc == 0 || nsm <= 0) return false;
     if (tc == 1 || p.batch > NM_MAX_BATCH) return true;
     const int64_t weights = p.rows * p.K;
     const int64_t per_sm = (p.rows + nsm - 1) / nsm;
@@ -268,6 +270,16 @@ bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
     if (p.batch >= 3) return weights > 24ll * 1000 * 1000;
     if (p.batch == 2) return weights >= (128ll << 20) && per_sm <= 128;
     return false;
+}
+
+bool takes_tensor_cores(const nm::SpmvProblem &p, uint32_t *lbo_enc)
+{
+    const int nsm = nm::sm_count();
+    if (nsm <= 0 || !nm::spmm_tc_applies(p, nsm)) {
+        nm::spmm_tc_mode(lbo_enc);
+        return false;
+    }
+    return takes_tensor_cores_rule(p, lbo_enc);
 }
 
 nm_status run_product(const nm::SpmvProblem &p, cudaStream_t s)
@@ -535,16 +547,35 @@ nm_status nm_spmv_group(const nm_matrix *A, int count, const void *const *x, int
         }
         ++g.count;
     }
-    // members that all take the tensor-core product (e.g. the 70B-shaped
-    // gate/up from batch 3) run as separate launches of it, faster than one
-    // fused CUDA-core launch (and above 8 vectors the only way)
-    bool all_tc = g.count > 0;
-    for (int i = 0; i < g.count && all_tc; ++i) {
-        uint32_t lbo = 0;
-        all_tc = takes_tensor_cores(g.p[i], &lbo);
-    }
+    // A group that the tensor-core product can run as a whole (every member
+    // 2:4 within its limits, and the rule of takes_tensor_cores met by the
+    // group's rows together) runs in one launch of it: the 70B-shaped q/k/v
+    // (8192 + 1024 + 1024 rows, K = 8192) takes 24.3 us at batch 3-8 there,
+    // against 25.6 / 29.2 us for one fused CUDA-core launch at batch 3 / 4
+    // and 33.4 us for three tensor-core launches at batch 8.  Failing that
+    // (no grouped plan fits: e.g. two 28672-row members), members that all
+    // take the tensor-core product alone run one launch each, and other
+    // groups one fused CUDA-core launch.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
+    uint32_t lbo = 0;
+    if (g.count > 1) {
+        nm::SpmvProblem whole = g.p[0];
+        whole.rows = 0;
+        const int nsm = nm::sm_count();
+        bool runs = nsm > 0;
+        for (int i = 0; i < g.count && runs; ++i) {
+            whole.rows += g.p[i].rows;
+            runs = nm::spmm_tc_applies(g.p[i], nsm);
+        }
+        if (runs && takes_tensor_cores_rule(whole, &lbo)) {
+            e = nm::launch_spmm_tc_group(g, nm::spmm_tc_desc_hi(lbo), s);
+            if (e == cudaSuccess) return NM_OK;
+            if (e != cudaErrorNotSupported) return cuda_fail(e, "nm_spmv_group launch");
+        }
+    }
+    bool all_tc = g.count > 0;
+    for (int i = 0; i < g.count && all_tc; ++i) all_tc = takes_tensor_cores(g.p[i], &lbo);
     if (fusable && !all_tc && g.count > 1 &&
         nm::bulk_path_applies(g.p[0].N, g.p[0].M, g.p[0].K))
         e = nm::launch_rows(g, s);

@@ -294,13 +294,14 @@ struct BulkTuning {
     int sp_tmem = 512;             // tensor-memory columns a CTA of it allocates (256 or 512)
     int sp_k = 0;                  // its K split's cluster size (0: chosen by shape)
     int sp_units = 0;              // its K split's row units at least (0: one a tile or tile pair)
+    int sp_group = 1;              // 1: a group's products in one launch of it; 0: one a product
 };
 
 // Tuning defaults, overridable by NM_BULK_TUNE="key=value,..." with keys
 // warps, cpl, R, stage, ring (bulk kernel), rows_warps, rows_R, rows_task,
 // rows_ring, rows_xtile, rows_pair, rows_pre, rows_prew, rows_l2pre, rows_two, rows (row-per-warp kernel),
 // ctas, pdl, wait_fault_test, tc_sp, sp_meta, sp_acc, sp_mbufs, sp_sel, sp_spin, sp_split,
-// sp_stages, sp_tmem, sp_k, sp_units
+// sp_stages, sp_tmem, sp_k, sp_units, sp_group
 // (both), tc, tc_lbo (tensor-core product); read once per process.
 const BulkTuning &bulk_tuning();
 
@@ -319,6 +320,21 @@ struct SpSplit {
 // where the cost model is described).  resident[k] (k = 2, 4, 8): clusters
 // of k CTAs resident at once on the device (0: none).
 SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *resident);
+
+// The same for `count` (<= 8) products with the same K and batch in one
+// launch: units[i] row units of matrix i (consecutive, matrix 0 first), its
+// rows spread evenly over them (box_rows[i] rows at most).  With one matrix
+// it is sp_split_plan's plan.
+struct SpGroupPlan {
+    int k;
+    int count;
+    int64_t units[8];
+    int box_rows[8];
+    int64_t total_units;
+    int max_box_rows;
+};
+SpGroupPlan sp_group_plan(const int64_t *rows, int count, int64_t K, int batch, int nsm,
+                          const int *resident);
 
 struct BulkPlan {
     int W, cpl, ktiles, tile_chunks, R, S, grid;

@@ -58,6 +58,7 @@ BulkTuning parse_tuning()
         else if (!std::strcmp(tok, "sp_tmem") && (v == 256 || v == 512)) t.sp_tmem = v;
         else if (!std::strcmp(tok, "sp_k") && v >= 0 && v <= 8 && v != 1) t.sp_k = v;
         else if (!std::strcmp(tok, "sp_units") && v >= 0) t.sp_units = v;
+        else if (!std::strcmp(tok, "sp_group") && (v == 0 || v == 1)) t.sp_group = v;
         else if (!std::strcmp(tok, "rows_l2pre") && v >= 0) t.rows_l2pre_bytes = v;
         else if (!std::strcmp(tok, "tc") && (v == -1 || v == 0 || v == 1)) t.tc = v;
         else if (!std::strcmp(tok, "tc_lbo") && v >= 0 && v < 16384) t.tc_lbo = v;
@@ -440,9 +441,11 @@ bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, 
     return rows_plan_impl(rpc, used, chunks, CK, B, max_smem, max_warps, out, false, tab_bytes);
 }
 
-// The sparse-operand tensor-core product's plan.  Without the split the rows
-// are spread over min(rows, nsm) CTAs; with it, units of one or two 128-row
-// tiles are each shared by a cluster of k = 2, 4 or 8 CTAs (rank 0 receives
+// The sparse-operand tensor-core product's plan, for one matrix or a group
+// launched together.  Without the split the rows are spread over min(rows,
+// nsm) CTAs (a group's CTAs split over its matrices in proportion to their
+// rows); with it, units of one or two 128-row tiles are each shared by a
+// cluster of k = 2, 4 or 8 CTAs (rank 0 receives
 // the other ranks' sums, 8, 16 or 32 floats a row by the batch, in at most
 // 64 KB of shared memory).
 // Measured on B300: a CTA's 128-position slab costs ~0.43 us with one tile
@@ -456,48 +459,93 @@ bool rows_plan_group(const int64_t *rows, int count, int chunks, int CK, int B, 
 // of its size are resident.  Tuning keys: sp_split=0 (never split), sp_k
 // (only that cluster size, taken wherever it fits), sp_units (at least that
 // many units).
-SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *resident)
+SpGroupPlan sp_group_plan(const int64_t *rows, int count, int64_t K, int batch, int nsm,
+                          const int *resident)
 {
     constexpr int kTile = 128;  // rows of an MMA tile
     constexpr int kSlab = 128;  // K positions of a slab
     const int64_t nslab = K / kSlab;
-    const double bytes = static_cast<double>(rows) * static_cast<double>(K) * 1.125;
-    auto estimate = [&](int k, int64_t units, int box_rows) {
-        const int nt = (box_rows + kTile - 1) / kTile;
-        const double t_slab = static_cast<double>((nslab + k - 1) / k) * (nt == 1 ? 0.43 : 0.61);
-        const double ctas = static_cast<double>(units * k);
+    int64_t total_rows = 0;
+    for (int i = 0; i < count; ++i) total_rows += rows[i];
+    const double bytes = static_cast<double>(total_rows) * static_cast<double>(K) * 1.125;
+    auto finish = [&](SpGroupPlan &g) {
+        g.total_units = 0;
+        g.max_box_rows = 0;
+        for (int i = 0; i < g.count; ++i) {
+            g.box_rows[i] = static_cast<int>((rows[i] + g.units[i] - 1) / g.units[i]);
+            g.total_units += g.units[i];
+            g.max_box_rows = std::max(g.max_box_rows, g.box_rows[i]);
+        }
+    };
+    auto estimate = [&](const SpGroupPlan &g) {
+        const int nt = (g.max_box_rows + kTile - 1) / kTile;
+        const double t_slab = static_cast<double>((nslab + g.k - 1) / g.k) * (nt == 1 ? 0.43 : 0.61);
+        const double ctas = static_cast<double>(g.total_units * g.k);
         const double t_bw = std::max(bytes / 6.2e6, bytes / (ctas * 55e3));
         return std::max(t_slab, t_bw);
     };
-    SpSplit best;
+    // no split: min(total rows, nsm) CTAs, each matrix at least one and a
+    // share in proportion to its rows (never more CTAs than rows)
+    SpGroupPlan best = {};
     best.k = 1;
-    best.units = std::max<int64_t>(1, std::min<int64_t>(rows, nsm));
-    best.box_rows = static_cast<int>((rows + best.units - 1) / best.units);
-    double t_best = estimate(1, best.units, best.box_rows);
+    best.count = count;
+    const int64_t ctas = std::max<int64_t>(count, std::min<int64_t>(total_rows, nsm));
+    int64_t used = 0;
+    for (int i = 0; i < count; ++i) {
+        const int64_t share = total_rows > 0 ? ctas * rows[i] / total_rows : 1;
+        best.units[i] = std::max<int64_t>(1, std::min<int64_t>(rows[i], share));
+        used += best.units[i];
+    }
+    while (used < ctas) {  // the rest to the matrices with the most rows a CTA
+        int at = -1;
+        for (int i = 0; i < count; ++i)
+            if (best.units[i] < rows[i] &&
+                (at < 0 || rows[i] * best.units[at] > rows[at] * best.units[i]))
+                at = i;
+        if (at < 0) break;
+        ++best.units[at];
+        ++used;
+    }
+    finish(best);
+    double t_best = estimate(best);
     const BulkTuning &tu = bulk_tuning();
-    if (!tu.sp_split || batch > 32 || rows < 1) return best;
+    if (!tu.sp_split || batch > 32 || total_rows < 1) return best;
     const int row_bytes = batch <= 8 ? 32 : batch <= 16 ? 64 : 128;  // a rank's sums of a row
     for (int k = 2; k <= 8; k *= 2) {
         if (tu.sp_k > 0 && k != tu.sp_k) continue;
         if (k > nslab) break;
         for (int nt = 1; nt <= 2; ++nt) {
-            int64_t units = (rows + kTile * nt - 1) / (kTile * nt);
-            if (tu.sp_units > 0) units = std::max<int64_t>(units, std::min<int64_t>(tu.sp_units, rows));
-            if (units * k > nsm || units > resident[k]) continue;
+            SpGroupPlan g = {};
+            g.k = k;
+            g.count = count;
+            for (int i = 0; i < count; ++i) {
+                g.units[i] = (rows[i] + kTile * nt - 1) / (kTile * nt);
+                if (tu.sp_units > 0 && count == 1)
+                    g.units[i] = std::max<int64_t>(g.units[i], std::min<int64_t>(tu.sp_units, rows[i]));
+            }
+            finish(g);
+            if (g.total_units * k > nsm || g.total_units > resident[k]) continue;
+            if (g.max_box_rows > kTile * nt) continue;
             // rank 0's region for the other ranks' sums stays within 64 KB
             if ((k - 1) * kTile * nt * row_bytes > 65536) continue;
-            const int box_rows = static_cast<int>((rows + units - 1) / units);
-            if (box_rows > kTile * nt) continue;
-            const double t = estimate(k, units, box_rows);
+            const double t = estimate(g);
             if (t < 0.97 * t_best || (tu.sp_k > 0 && best.k == 1)) {
-                best.k = k;
-                best.units = units;
-                best.box_rows = box_rows;
+                best = g;
                 t_best = t;
             }
         }
     }
     return best;
+}
+
+SpSplit sp_split_plan(int64_t rows, int64_t K, int batch, int nsm, const int *resident)
+{
+    const SpGroupPlan g = sp_group_plan(&rows, 1, K, batch, nsm, resident);
+    SpSplit p;
+    p.k = g.k;
+    p.units = g.units[0];
+    p.box_rows = g.box_rows[0];
+    return p;
 }
 
 }  // namespace nm

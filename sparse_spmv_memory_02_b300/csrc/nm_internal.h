@@ -86,6 +86,11 @@ uint64_t calib_desc_hi(uint32_t lbo, uint32_t sbo);
 // operands' shared-memory descriptor fields (spmm_tc_desc_hi(1)).
 bool spmm_tc_applies(const SpmvProblem &p, int nsm);
 cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s);
+// The products of a group (same K, batch, x stride and y type; each as
+// spmm_tc_applies allows) in one launch of the sparse-operand product;
+// cudaErrorNotSupported when that kernel is not the one selected (tc_sp=0,
+// sp_group=0) or no plan fits: the caller then launches them one by one.
+cudaError_t launch_spmm_tc_group(const SpmvGroup &g, uint64_t desc_hi, cudaStream_t s);
 uint32_t spmm_tc_idesc(int N);
 // When products take that path (tuning key tc: 1 wherever it applies, 0
 // never, -1 by batch and layer size: takes_tensor_cores in nm_api.cu) and

@@ -511,11 +511,32 @@ __host__ __device__ constexpr uint32_t sp_meta_col(uint32_t meta_base, int ntile
     return meta_base + 8u * static_cast<uint32_t>((d * ntile + t) * 4 + kk);
 }
 
-struct SpArgs {
+constexpr int kSpMaxGroup = 8;         // matrices one launch may stream (a group's)
+
+// One matrix of a launch: its rows are spread evenly over its row units
+// [unit_begin, unit_begin + units) (CTAs, or clusters with the K split);
+// its boxes carry box_rows rows.
+struct SpMat {
     void *y;
     int64_t ldy;
-    int rows, K, batch, Np;
-    int row_base, row_extra;
+    int row_base, row_extra;   // rows of unit u: row_base (+1 if u < row_extra)
+    int unit_begin;            // first unit (units of all matrices in order)
+    int box_rows;
+    int x3d;                   // 1: x through the 3-D map
+};
+
+// The tensor maps of each matrix (values, mask words, x).
+struct SpMaps {
+    CUtensorMap v[kSpMaxGroup];
+    CUtensorMap m[kSpMaxGroup];
+    CUtensorMap x[kSpMaxGroup];
+};
+
+struct SpArgs {
+    SpMat mat[kSpMaxGroup];
+    int nmat;
+    int total_units;          // row units of all matrices (grid = total_units * ksplit)
+    int K, batch, Np;
     int y_f32;
     uint32_t idesc;           // tcgen05 instruction descriptor, sparse bit set
     uint64_t desc_hi;         // K-major, 128-byte swizzle, SBO 1024 (A and B)
@@ -523,7 +544,6 @@ struct SpArgs {
     int S;                    // ring stages
     int off_m, off_x;         // masks and x inside a stage (values at 0, ntile * 16 KB)
     int stage_bytes, x_bytes, off_bar;
-    int x3d;
     int meta_mode;            // sp_meta_word mode
     int ksplit;               // CTAs (one cluster) sharing a unit of rows, each a part of K
                               // (1: no split, rows split evenly over the CTAs)
@@ -613,23 +633,28 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t r0, uint32_t r
 }
 
 __global__ void __launch_bounds__(kSpThreads, 1)
-nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
-                  const __grid_constant__ CUtensorMap tm_masks,
-                  const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ SpArgs a)
+nm_spmm_sp_kernel(const __grid_constant__ SpMaps maps, const __grid_constant__ SpArgs a)
 {
     extern __shared__ __align__(1024) uint8_t sp_smem_raw[];
     uint8_t *smem = sp_smem_raw;
     // every operand region starts 1024-byte aligned (swizzled boxes, MMA
-    // descriptors) and the metadata columns fit the allocation: else nothing
-    if (((smem_addr(sp_smem_raw) | a.stage_bytes | a.off_m | a.off_x) & 1023u) ||
+    // descriptors), the metadata columns fit the allocation and every
+    // matrix's boxes fit the stages' tiles: else nothing (the same for all
+    // CTAs, before any barrier)
+    bool bad_mat = a.nmat < 1 || a.nmat > kSpMaxGroup || a.total_units < 1 ||
+                   gridDim.x != static_cast<unsigned>(a.total_units * a.ksplit);
+    for (int i = 0; i < a.nmat && !bad_mat; ++i)
+        bad_mat = a.mat[i].box_rows < 1 || a.mat[i].box_rows > kTileM * a.ntile ||
+                  a.mat[i].row_base + (a.mat[i].row_extra ? 1 : 0) > a.mat[i].box_rows ||
+                  a.mat[i].unit_begin < 0 || a.mat[i].unit_begin >= a.total_units;
+    if (bad_mat || ((smem_addr(sp_smem_raw) | a.stage_bytes | a.off_m | a.off_x) & 1023u) ||
         a.S < 2 || a.S > kSpMaxStages ||
         a.nmbuf < 1 || a.nmbuf > kSpMaxMetaBufs || a.nacc < 1 || a.nacc > kSpMaxAccSets ||
         a.meta_base < static_cast<uint32_t>(4 * a.nacc * a.Np) ||
         (a.tmem_cols != 256 && a.tmem_cols != kSpTmemCols) ||
         sp_meta_col(a.meta_base, a.ntile, a.nmbuf - 1, a.ntile - 1, 3) >= a.tmem_cols ||
         (a.ksplit > 1 &&
-         (a.ksplit > 8 || gridDim.x % a.ksplit != 0 ||
-          a.row_base + (a.row_extra ? 1 : 0) > kTileM * a.ntile ||
+         (a.ksplit > 8 ||
           (a.split_cols != 8 && a.split_cols != 16 && a.split_cols != 32) ||
           a.batch > a.split_cols || a.split_cols > a.Np ||
           a.K / kSlabPos < a.ksplit || (a.off_part & 15) ||
@@ -663,8 +688,12 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     // the split).
     const int rank = a.ksplit > 1 ? cta % a.ksplit : 0;
     const int unit = cta / a.ksplit;
-    const int r_begin = unit * a.row_base + min(unit, a.row_extra);
-    const int r_count = a.row_base + (unit < a.row_extra ? 1 : 0);
+    int mi = 0;  // the matrix of this unit (units of a matrix are consecutive)
+    while (mi + 1 < a.nmat && unit >= a.mat[mi + 1].unit_begin) ++mi;
+    const SpMat &mt = a.mat[mi];
+    const int lu = unit - mt.unit_begin;  // unit within the matrix
+    const int r_begin = lu * mt.row_base + min(lu, mt.row_extra);
+    const int r_count = mt.row_base + (lu < mt.row_extra ? 1 : 0);
     const int ntile = (r_count + kTileM - 1) / kTileM;  // this CTA's tiles (<= a.ntile)
     const int nconv = 4 * ntile;                        // metadata warps at work
     const int nslab_all = a.K / kSlabPos;
@@ -676,7 +705,8 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
     const int Q = max(S, NB) + 1;  // exceeds both ring depths
 
     // the tensor maps' descriptors start on their way now
-    if (warp == kSpProdWarp && lane < 3) prefetch_map(lane == 0 ? &tm_vals : lane == 1 ? &tm_masks : &tm_x);
+    const CUtensorMap *tm_vals = &maps.v[mi], *tm_masks = &maps.m[mi], *tm_x = &maps.x[mi];
+    if (warp == kSpProdWarp && lane < 3) prefetch_map(lane == 0 ? tm_vals : lane == 1 ? tm_masks : tm_x);
     // one thread a barrier (Q exceeds S and NB)
     if (static_cast<int>(threadIdx.x) < Q) {
         const int i = threadIdx.x;
@@ -738,7 +768,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
             const uint64_t pol = l2_evict_first_policy();
             const int slab0 = static_cast<int>((static_cast<int64_t>(cta) * nslab) / gridDim.x) %
                               max(nslab, 1);
-            const uint32_t box_rows = static_cast<uint32_t>(a.row_base + (a.row_extra ? 1 : 0));
+            const uint32_t box_rows = static_cast<uint32_t>(mt.box_rows);
             const uint32_t tx = role == 0 ? box_rows * 128u
                               : role == 1 ? box_rows * 16u
                                           : static_cast<uint32_t>(a.x_bytes);
@@ -762,14 +792,14 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 ks += slab_lo;
                 mbar_arrive_expect_tx(&full[s], tx);
                 if (role == 0) {
-                    tma2d_hint(st, &tm_vals, ks * 64, r_begin, &full[s], pol);
+                    tma2d_hint(st, tm_vals, ks * 64, r_begin, &full[s], pol);
                 } else if (role == 1) {
-                    tma2d_hint(st + a.off_m, &tm_masks, ks * 4, r_begin, &full[s], pol);
-                } else if (a.x3d) {
-                    tma3d(st + a.off_x, &tm_x, 0, 0, 2 * ks, &full[s]);
+                    tma2d_hint(st + a.off_m, tm_masks, ks * 4, r_begin, &full[s], pol);
+                } else if (mt.x3d) {
+                    tma3d(st + a.off_x, tm_x, 0, 0, 2 * ks, &full[s]);
                 } else {
-                    tma2d(st + a.off_x, &tm_x, ks * kSlabPos, 0, &full[s]);
-                    tma2d(st + a.off_x + a.x_bytes / 2, &tm_x, ks * kSlabPos + 64, 0, &full[s]);
+                    tma2d(st + a.off_x, tm_x, ks * kSlabPos, 0, &full[s]);
+                    tma2d(st + a.off_x + a.x_bytes / 2, tm_x, ks * kSlabPos + 64, 0, &full[s]);
                 }
                 ++issued;
                 if (++s == S) s = 0;
@@ -979,7 +1009,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
                 if (go && landed && row < r_count) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (j < a.batch) store_y(a.y, j * a.ldy + r_begin + row, v[j], a.y_f32 != 0);
+                        if (j < a.batch) store_y(mt.y, j * mt.ldy + r_begin + row, v[j], a.y_f32 != 0);
                 }
             }
         }
@@ -1006,7 +1036,7 @@ nm_spmm_sp_kernel(const __grid_constant__ CUtensorMap tm_vals,
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (b0 + j < a.batch)
-                        store_y(a.y, (b0 + j) * a.ldy + r_begin + row, v[j], a.y_f32 != 0);
+                        store_y(mt.y, (b0 + j) * mt.ldy + r_begin + row, v[j], a.y_f32 != 0);
             }
         }
     }
@@ -1143,17 +1173,29 @@ int sp_resident_clusters(int k)
     return n;
 }
 
-// The split plan for this device: its resident cluster counts for k = 2, 4, 8.
-SpSplit sp_plan(const SpmvProblem &p, int nsm)
+// The plan for these products on this device (its resident cluster counts
+// for k = 2, 4, 8).
+SpGroupPlan sp_plan(const SpmvProblem *ps, int count, int nsm)
 {
     int resident[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
     for (int k = 2; k <= 8; k *= 2) resident[k] = sp_resident_clusters(k);
-    return sp_split_plan(p.rows, p.K, p.batch, nsm, resident);
+    int64_t rows[kSpMaxGroup];
+    for (int i = 0; i < count; ++i) rows[i] = ps[i].rows;
+    return sp_group_plan(rows, count, ps[0].K, ps[0].batch, nsm, resident);
 }
 
-// The sparse-operand variant (nm_spmm_sp_kernel); same maps and conditions.
-cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode, cudaStream_t s)
+// The sparse-operand variant (nm_spmm_sp_kernel) for `count` products with
+// the same K, batch, x stride and y type in one launch (each as
+// spmm_tc_applies allows); one product is a group of one.
+cudaError_t launch_spmm_sp_group(const SpmvProblem *ps, int count, uint64_t desc_hi, int meta_mode,
+                                 cudaStream_t s)
 {
+    if (count < 1 || count > kSpMaxGroup) return cudaErrorNotSupported;
+    const SpmvProblem &p = ps[0];
+    for (int i = 1; i < count; ++i)
+        if (ps[i].K != p.K || ps[i].batch != p.batch || ps[i].ldx != p.ldx ||
+            ps[i].y_f32 != p.y_f32)
+            return cudaErrorNotSupported;
     EncodeTiled enc = encode_tiled_tc();
     if (!enc) return cudaErrorNotSupported;
     const int nsm = sm_count();
@@ -1161,41 +1203,49 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     const int Np = p.batch <= 16 ? 16 : 32;
     const int64_t Lv = p.K / 2;
     const int64_t Lm = p.K / 32;
-    const SpSplit plan = sp_plan(p, nsm);
-    if (plan.box_rows > kMaxRows) return cudaErrorNotSupported;
+    const SpGroupPlan plan = sp_plan(ps, count, nsm);
+    if (plan.max_box_rows > kMaxRows) return cudaErrorNotSupported;
     const int ksplit = plan.k;
-    const int64_t units = plan.units;  // row units: CTAs, or clusters with the split
-    const int grid = static_cast<int>(units) * ksplit;
-    const int box_rows = plan.box_rows;
-    CUtensorMap tv, tm, tx;
-    if (!encode2d(enc, &tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.values, Lv, p.rows, Lv * 2, 64,
-                  box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode2d(enc, &tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, p.masks, Lm, p.rows, Lm * 4, 4,
-                  box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorNotSupported;
+    const int grid = static_cast<int>(plan.total_units) * ksplit;
+    const int box_rows = plan.max_box_rows;  // the stages' layout
     // x: only the batch's rows, rounded up to 8 (one 128-byte-swizzle atom);
     // the MMA reads Np rows, and the rows past Bx read whatever follows: they
     // only feed accumulator columns that are never stored
     const int Bx = (p.batch + 7) / 8 * 8;
-    int x3d = 1;
-    if (!encode_x3d(enc, &tx, p.x, p.K, p.batch, p.ldx * 2, Bx)) {
-        x3d = 0;
-        if (!encode2d(enc, &tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, p.x, p.K, p.batch, p.ldx * 2, 64,
-                      Bx, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorNotSupported;
-    }
+    SpMaps maps;
     SpArgs a = {};
-    a.x3d = x3d;
-    a.y = p.y;
-    a.ldy = p.ldy;
-    a.rows = static_cast<int>(p.rows);
+    int64_t unit = 0;
+    for (int i = 0; i < count; ++i) {
+        const SpmvProblem &q = ps[i];
+        const int br = plan.box_rows[i];
+        if (!encode2d(enc, &maps.v[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, q.values, Lv, q.rows,
+                      Lv * 2, 64, br, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode2d(enc, &maps.m[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, q.masks, Lm, q.rows,
+                      Lm * 4, 4, br, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorNotSupported;
+        SpMat &m = a.mat[i];
+        m.x3d = 1;
+        if (!encode_x3d(enc, &maps.x[i], q.x, q.K, q.batch, q.ldx * 2, Bx)) {
+            m.x3d = 0;
+            if (!encode2d(enc, &maps.x[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, q.x, q.K, q.batch,
+                          q.ldx * 2, 64, Bx, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorNotSupported;
+        }
+        m.y = q.y;
+        m.ldy = q.ldy;
+        // rows spread evenly over the matrix's units (CTAs, or clusters with
+        // the K split); a box carries row_base (+1) rows
+        m.row_base = static_cast<int>(q.rows / plan.units[i]);
+        m.row_extra = static_cast<int>(q.rows % plan.units[i]);
+        m.unit_begin = static_cast<int>(unit);
+        m.box_rows = br;
+        unit += plan.units[i];
+    }
+    a.nmat = count;
+    a.total_units = static_cast<int>(plan.total_units);
     a.K = static_cast<int>(p.K);
     a.batch = p.batch;
     a.Np = Np;
-    // rows spread evenly over the units (CTAs, or the tiles with the K
-    // split); a box carries row_base (+1) rows
-    a.row_base = static_cast<int>(p.rows / units);
-    a.row_extra = static_cast<int>(p.rows % units);
     a.y_f32 = p.y_f32 ? 1 : 0;
     a.idesc = spmm_tc_idesc(Np) | (1u << 2);  // sparse A
     a.desc_hi = desc_hi;
@@ -1261,7 +1311,18 @@ cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    return cudaLaunchKernelEx(&cfg, nm_spmm_sp_kernel, tv, tm, tx, a);
+    return cudaLaunchKernelEx(&cfg, nm_spmm_sp_kernel, maps, a);
+}
+
+cudaError_t launch_spmm_sp(const SpmvProblem &p, uint64_t desc_hi, int meta_mode, cudaStream_t s)
+{
+    return launch_spmm_sp_group(&p, 1, desc_hi, meta_mode, s);
+}
+
+cudaError_t launch_spmm_tc_group(const SpmvGroup &g, uint64_t desc_hi, cudaStream_t s)
+{
+    if (!bulk_tuning().tc_sp || !bulk_tuning().sp_group) return cudaErrorNotSupported;
+    return launch_spmm_sp_group(g.p, g.count, desc_hi, bulk_tuning().sp_meta, s);
 }
 
 cudaError_t launch_spmm_tc(const SpmvProblem &p, uint64_t desc_hi, cudaStream_t s)

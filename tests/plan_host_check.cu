@@ -174,6 +174,43 @@ void sp_one(int64_t rows, int64_t K, int B, const int *resident, const char *dev
     }
 }
 
+// A group's plan: every matrix at least one unit and at most one a row, its
+// rows spread over its units, at most one CTA an SM, the split's limits as
+// for one matrix; a group of one has sp_split_plan's plan.
+void sp_group_one(const std::vector<int64_t> &rows, int64_t K, int B, const int *resident,
+                  const char *dev)
+{
+    const nm::SpGroupPlan g = nm::sp_group_plan(rows.data(), static_cast<int>(rows.size()), K, B,
+                                                kNsm, resident);
+    ++g_plans;
+    int64_t total = 0, total_rows = 0;
+    int maxb = 0;
+    for (size_t i = 0; i < rows.size(); ++i) {
+        EXPECT(g.units[i] >= 1 && g.units[i] <= std::max<int64_t>(1, rows[i]),
+               "%s group %zu: units %lld rows %lld", dev, i, (long long)g.units[i],
+               (long long)rows[i]);
+        EXPECT(g.box_rows[i] == static_cast<int>((rows[i] + g.units[i] - 1) / g.units[i]),
+               "%s group %zu: box %d", dev, i, g.box_rows[i]);
+        total += g.units[i];
+        total_rows += rows[i];
+        maxb = std::max(maxb, g.box_rows[i]);
+    }
+    EXPECT(g.count == static_cast<int>(rows.size()) && g.total_units == total &&
+               g.max_box_rows == maxb && total * g.k <= std::max<int64_t>(kNsm, total),
+           "%s group totals: units %lld k %d", dev, (long long)total, g.k);
+    if (g.k > 1) {
+        const int nt = (maxb + 127) / 128;
+        EXPECT(B <= 32 && total * g.k <= kNsm && total <= resident[g.k] && g.k <= K / 128 &&
+                   maxb <= 256 && (g.k - 1) * 128 * nt * (B <= 8 ? 32 : B <= 16 ? 64 : 128) <= 65536,
+               "%s group split k %d units %lld box %d", dev, g.k, (long long)total, maxb);
+    }
+    if (rows.size() == 1) {
+        const nm::SpSplit p = nm::sp_split_plan(rows[0], K, B, kNsm, resident);
+        EXPECT(p.k == g.k && p.units == g.units[0] && p.box_rows == g.box_rows[0],
+               "%s group of one differs from the single plan", dev);
+    }
+}
+
 // Plans the B300 measurements chose (resident clusters of 2, 4, 8: 74, 37,
 // 18), at batch 8 with the default tuning.
 void sp_expect(int64_t rows, int64_t K, int k, int64_t units)
@@ -215,6 +252,16 @@ int main()
                 sp_one(r, K, B, res_b300, "b300");
                 sp_one(r, K, B, res_small, "small");
                 sp_one(r, K, B, res_none, "none");
+            }
+    const std::vector<std::vector<int64_t>> sp_groups = {
+        {8192, 1024, 1024}, {4096, 1024, 1024}, {28672, 28672}, {1}, {5, 7},
+        {100000, 1}, {300, 77, 250, 4, 5, 6, 7, 900}, {8192}, {20000, 20000}};
+    for (auto &g : sp_groups)
+        for (int64_t K : {128L, 1024L, 8192L})
+            for (int B : {3, 8, 16, 32}) {
+                sp_group_one(g, K, B, res_b300, "b300");
+                sp_group_one(g, K, B, res_small, "small");
+                sp_group_one(g, K, B, res_none, "none");
             }
     if (nm::bulk_tuning().sp_split && nm::bulk_tuning().sp_k == 0 &&
         nm::bulk_tuning().sp_units == 0) {

@@ -128,6 +128,47 @@ def test_tensor_core_path_above_batch_8(rows, K, B):
     assert nm.nm_device_errors() == 0
 
 
+def _group_check(rows_list, K, B, seed):
+    """nm_spmv_group over matrices of these rows, each with its own x, against
+    the oracle on sampled rows of every member."""
+    Ws, masks, mats, xs = [], [], [], []
+    for i, rows in enumerate(rows_list):
+        W = nm_synth.weights(rows, K, seed + i, DEV)
+        mask = nm_synth.topn_mask(W, 2, 4)
+        Ws.append(W)
+        masks.append(mask)
+        mats.append(nm.nm_pack(W, mask, 2, 4))
+        xs.append(nm_synth.activations(K, B, seed + 50 + i, True, DEV))
+    ys = nm.nm_spmv_group(mats, xs, y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(seed)
+    for i, rows in enumerate(rows_list):
+        pick = np.sort(g.choice(rows, min(rows, 192), replace=False))
+        idx = torch.from_numpy(pick).to(DEV)
+        yr, sr = oracle.spmv_dense(Ws[i][idx].cpu().numpy().view(np.uint16),
+                                   masks[i][idx].cpu().numpy(), xs[i].cpu().numpy().view(np.uint16))
+        ok = oracle.within_tolerance(ys[i][:, idx].double().cpu().numpy(), yr, sr)
+        assert ok.all(), "member %d (%d rows): %d/%d outside tolerance" % (
+            i, rows, (~ok).sum(), ok.size)
+    assert nm.nm_device_errors() == 0
+
+
+@pytest.mark.parametrize("B", [9, 16, 32])
+@pytest.mark.parametrize("rows_list", [(8192, 1024, 1024), (300, 77, 250, 4, 5), (1000, 2048)],
+                         ids=["qkv_shaped", "ragged5", "two"])
+def test_group_in_one_tensor_core_launch(rows_list, B):
+    """Above 8 vectors every 2:4 member takes the tensor-core product, so a
+    group is one grouped launch of it (units of each matrix consecutive,
+    each matrix its own maps, x and y): each member against the oracle."""
+    _group_check(rows_list, 1024, B, 300 + B)
+
+
+def test_group_70b_qkv_batch8_one_launch():
+    """The 70B-shaped q/k/v (8192 + 1024 + 1024 rows, K = 8192) at batch 8:
+    all three take the tensor cores, in one grouped launch."""
+    _group_check((8192, 1024, 1024), 8192, 8, 77)
+
+
 def test_batch_above_8_unsupported_where_the_tensor_cores_cannot_run():
     """257 rows per SM exceed the tensor-core product's two tiles: batch 9
     is refused (NM_ERR_UNSUPPORTED) before any launch, batch 8 runs on the
