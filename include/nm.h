@@ -224,10 +224,13 @@ nm_status nm_spmv_batched(const nm_matrix *A, const void *x, int64_t ldx,
  *   batch, ldx, y_type, stream: as nm_spmv_batched, shared by all products.
  * Each product's arguments are checked as by nm_spmv_batched (errors name
  * the matrix); matrices that differ in N, M or K are NM_ERR_INVALID_ARG.
- * When the shapes cannot share a launch, or every product takes the
- * tensor-core path of nm_spmv_batched, the products are launched one by one,
- * with the same results (then each on the kernel nm_spmv_batched picks); a
- * batch above NM_MAX_BATCH needs every product to take that path.
+ * A 2:4 group that the tensor-core path of nm_spmv_batched can run as a
+ * whole (every member within its limits, the group's rows together meeting
+ * its routing rule) is one launch of that path; otherwise the products share
+ * one CUDA-core launch when they can, or are launched one by one (then each
+ * on the kernel nm_spmv_batched picks).  Results are within the same error
+ * bound and deterministic for a given group; a batch above NM_MAX_BATCH needs
+ * every product to be one the tensor-core path runs.
  * Asynchronous, allocates nothing, may be captured in a CUDA graph; the
  * products' y must not overlap.
  */
