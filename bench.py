@@ -78,7 +78,7 @@ def parse_args(argv=None):
                    help="skip the batch crossover against 2:4 sparse tensor cores")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the other workloads (single layer, Qwen3-14B MLP pattern sweep, "
-                        "Llama-3.3-70B block at batch 1/2/4/8, 448-layer Qwen3-32B stream)")
+                        "Llama-3.3-70B block at batch 1/2/3/4/8, 448-layer Qwen3-32B stream)")
     p.add_argument("--calib-tokens", type=int, default=512,
                    help="decode-step tokens per nm_calib_accumulate call in the calibration timing")
     p.add_argument("--layer", default=None, metavar="ROWSxK",
@@ -766,7 +766,7 @@ def e2e_pass(layers, copies, steps, warmup, fused, silu=False, per_graph=1):
 # stream (the Llama-3.1-8B-shaped block is the headline itself).
 CONFIG_SET = ([("1", "single_1024", "2:4", 1)] +
               [("3", "qwen3_14b_mlp", p, 1) for p in ("2:4", "4:8", "1:4", "2:8")] +
-              [("4", "llama33_70b_block", "2:4", b) for b in (1, 2, 4, 8)] +
+              [("4", "llama33_70b_block", "2:4", b) for b in (1, 2, 3, 4, 8)] +
               [("5", "qwen3_32b_stream", "2:4", 1)])
 NOMINAL_HBM_GBS = 8000.0
 

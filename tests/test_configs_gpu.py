@@ -106,7 +106,7 @@ def test_config3_qwen3_14b_mlp_pattern_sweep(N, M):
         _check_layer(wl, L, N, M, 1)
 
 
-@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 8])
 def test_config4_llama33_70b_block_batched(batch):
     wl = nm_synth.WORKLOADS["llama33_70b_block"]
     layers, _ = _run_step(wl, 2, 4, batch)
