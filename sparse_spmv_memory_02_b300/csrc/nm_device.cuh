@@ -124,10 +124,14 @@ __host__ __device__ __forceinline__ float fma_h2(uint32_t v, uint32_t x, float a
         : "r"(v), "r"(x));
     return acc;
 #else
-    const float2 vf = __half22float2(*reinterpret_cast<const __half2 *>(&v));
-    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x));
-    acc = fmaf(vf.x, xf.x, acc);
-    return fmaf(vf.y, xf.y, acc);
+    // the halves by value (no pointer cast: the host compiler's aliasing
+    // rules forbid reading a uint32_t through a __half2)
+    const float vl = __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+    const float vh = __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+    const float xl = __half2float(__ushort_as_half(static_cast<unsigned short>(x & 0xFFFFu)));
+    const float xh = __half2float(__ushort_as_half(static_cast<unsigned short>(x >> 16)));
+    acc = fmaf(vl, xl, acc);
+    return fmaf(vh, xh, acc);
 #endif
 }
 
