@@ -492,6 +492,13 @@ nm_spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_vals,
 //     its own accumulator columns, and commit once a slab;
 //   * warps 0-7 read the accumulators, add the issuers' partial sums and
 //     round into y.
+// A launch covers one matrix or a group of up to 8 with the same K and
+// batch: each matrix's rows are spread evenly over its row units, and the
+// units of all matrices are numbered in order.  A unit is one CTA, or with
+// the K split one cluster of 2, 4 or 8 CTAs sharing a unit's one or two
+// 128-row tiles, each streaming a share of K's slabs; ranks 1.. send their
+// fp32 sums to rank 0 (st.async into its shared memory, counted on an
+// mbarrier), which adds them in rank order.  sp_group_plan picks the layout.
 constexpr int kSpConvWarps = 8;
 constexpr int kSpProdWarp = 8;        // warps 8-10: producers
 constexpr int kSpProdWarps = 3;
